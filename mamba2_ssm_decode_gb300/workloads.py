@@ -1,0 +1,281 @@
+"""Seeded synthetic inputs shaped like Mamba2 serving decode.
+
+This module only draws random tensors and slot tables; it holds none of the
+selective-state-update arithmetic.  Both the CUDA path and the CPU oracle are
+fed from it.  Value distributions (the same for every workload):
+
+  state    ~ N(0, 0.1^2)            (std 0.1), in the state dtype
+  x, z     ~ N(0, 1)                in the io dtype (bf16 unless stated)
+  B, C     ~ N(0, 1)                [rows, groups, dstate], io dtype
+  dt       ~ N(0, 1)                fp32, per head [rows, heads] unless dt_per_dim
+  dt_bias  ~ U[-4, -1]              fp32 per head
+  A        = -exp(U[0, ln 16])      fp32 per head, so A in [-16, -1]
+  D        ~ U[0, 1]                fp32 per head
+
+Slot tables are random subsets of the slot pool (distinct slots), with a
+seeded choice of sequences whose slots are replaced by the pad id.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+PAD_SLOT_ID = -1
+
+
+@dataclasses.dataclass
+class SSUCase:
+    """One call's inputs.  `kind` is "single" (one token per sequence) or "varlen"."""
+
+    kind: str
+    name: str
+    state: torch.Tensor                 # [slots, H, P, N]
+    x: torch.Tensor                     # [rows, H, P]
+    dt: torch.Tensor                    # [rows, H] or [rows, H, P] fp32
+    A: torch.Tensor                     # [H] fp32
+    B: torch.Tensor                     # [rows, G, N]
+    C: torch.Tensor                     # [rows, G, N]
+    D: torch.Tensor | None              # [H] fp32
+    dt_bias: torch.Tensor | None        # [H] fp32
+    z: torch.Tensor | None              # [rows, H, P]
+    state_batch_indices: torch.Tensor | None
+    dst_state_batch_indices: torch.Tensor | None = None
+    cu_seqlens: torch.Tensor | None = None
+    num_accepted_tokens: torch.Tensor | None = None
+    dense_steps: int = 1
+    nseqs: int = 0
+    pad_slot_id: int = PAD_SLOT_ID
+    dt_softplus: bool = True
+    disable_state_update: bool = False
+    # ReplaySSM trackers (int32 [num_states]) and their parameters, when the
+    # workload runs them
+    ring_start: torch.Tensor | None = None
+    prev_num_accepted: torch.Tensor | None = None
+    prev_query_len: torch.Tensor | None = None
+    logical_window: int = 0
+    ring_buffer_len: int = 1
+
+    @property
+    def rows(self) -> int:
+        return self.x.shape[0]
+
+    @property
+    def dims(self):
+        slots, H, P, N = self.state.shape
+        return slots, H, P, N, self.B.shape[1]
+
+    def tensors(self) -> dict:
+        return {f.name: getattr(self, f.name) for f in dataclasses.fields(self)
+                if isinstance(getattr(self, f.name), torch.Tensor)}
+
+    def to(self, device) -> "SSUCase":
+        kw = {}
+        for f in dataclasses.fields(self):
+            v = getattr(self, f.name)
+            kw[f.name] = v.to(device) if isinstance(v, torch.Tensor) else v
+        return SSUCase(**kw)
+
+    def clone(self) -> "SSUCase":
+        kw = {}
+        for f in dataclasses.fields(self):
+            v = getattr(self, f.name)
+            kw[f.name] = v.clone() if isinstance(v, torch.Tensor) else v
+        return SSUCase(**kw)
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _normal(shape, std, dtype, g, device):
+    t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(dtype)
+
+
+def _uniform(shape, lo, hi, g, device):
+    return torch.rand(shape, generator=g, device=device, dtype=torch.float32) * (hi - lo) + lo
+
+
+def _head_params(H, g, device):
+    A = -torch.exp(_uniform((H,), 0.0, math.log(16.0), g, device))
+    D = _uniform((H,), 0.0, 1.0, g, device)
+    dt_bias = _uniform((H,), -4.0, -1.0, g, device)
+    return A, D, dt_bias
+
+
+def _distinct_slots(count, slots, g, device):
+    if count > slots:
+        raise ValueError(f"need {count} distinct slots from a pool of {slots}")
+    return torch.randperm(slots, generator=g, device=device)[:count]
+
+
+def _pad_some(table, npad, pad, g, device):
+    """Replace the slots of `npad` seeded sequences (whole rows) by the pad id."""
+    if npad <= 0:
+        return table
+    who = torch.randperm(table.shape[0], generator=g, device=device)[:npad]
+    table = table.clone()
+    table[who] = pad
+    return table
+
+
+def single_token_case(*, batch, heads, headdim, dstate, groups, slots, state_dtype,
+                      io_dtype=torch.bfloat16, pad_frac=0.0, with_z=True, dt_per_dim=False,
+                      index_dtype=torch.int32, identity_slots=False, disable_state_update=False,
+                      seed=0, device="cpu", name="single") -> SSUCase:
+    g = _gen(seed, device)
+    state = _normal((slots, heads, headdim, dstate), 0.1, state_dtype, g, device)
+    x = _normal((batch, heads, headdim), 1.0, io_dtype, g, device)
+    dt_shape = (batch, heads, headdim) if dt_per_dim else (batch, heads)
+    dt = _normal(dt_shape, 1.0, torch.float32, g, device)
+    A, D, dt_bias = _head_params(heads, g, device)
+    B = _normal((batch, groups, dstate), 1.0, io_dtype, g, device)
+    C = _normal((batch, groups, dstate), 1.0, io_dtype, g, device)
+    z = _normal((batch, heads, headdim), 1.0, io_dtype, g, device) if with_z else None
+    if identity_slots:
+        sbi = torch.arange(batch, device=device)
+    else:
+        sbi = _distinct_slots(batch, slots, g, device)
+    sbi = _pad_some(sbi, round(pad_frac * batch), PAD_SLOT_ID, g, device).to(index_dtype)
+    return SSUCase(kind="single", name=name, state=state, x=x, dt=dt, A=A, B=B, C=C, D=D,
+                   dt_bias=dt_bias, z=z, state_batch_indices=sbi, nseqs=batch,
+                   disable_state_update=disable_state_update)
+
+
+def varlen_case(*, nseqs, max_len, heads, headdim, dstate, groups, slots, state_dtype,
+                io_dtype=torch.bfloat16, fixed_len=None, pad_frac=0.0, with_z=True,
+                dt_per_dim=False, index_dtype=torch.int32, meta_dtype=torch.int32,
+                same_tables=False, dense=False, with_trackers=False, logical_window=4,
+                ring_buffer_len=8, disable_state_update=False, seed=0, device="cpu",
+                name="varlen") -> SSUCase:
+    """Packed varlen MTP call.  Lengths are U{1..max_len} (or `fixed_len`), the
+    acceptance count of sequence s is U{1..len_s}; the read table and the write
+    table are [nseqs, max_len] of distinct slots (one table when same_tables)."""
+    g = _gen(seed, device)
+    if fixed_len is not None:
+        lens = torch.full((nseqs,), fixed_len, dtype=torch.int64, device=device)
+    else:
+        lens = torch.randint(1, max_len + 1, (nseqs,), generator=g, device=device)
+    cu = torch.zeros(nseqs + 1, dtype=torch.int64, device=device)
+    cu[1:] = torch.cumsum(lens, 0)
+    rows = int(cu[-1].item())
+    # acceptance count U{1..len}: floor(u * len) + 1
+    u = torch.rand((nseqs,), generator=g, device=device)
+    na = (torch.floor(u * lens.to(torch.float32)).to(torch.int64) + 1).clamp(max=lens)
+    ntab = 1 if same_tables else 2
+    perm = _distinct_slots(ntab * nseqs * max_len, slots, g, device)
+    sbi = perm[: nseqs * max_len].reshape(nseqs, max_len)
+    dsbi = sbi if same_tables else perm[nseqs * max_len:].reshape(nseqs, max_len)
+    npad = round(pad_frac * nseqs)
+    if npad:
+        who = torch.randperm(nseqs, generator=g, device=device)[:npad]
+        sbi = sbi.clone()
+        sbi[who] = PAD_SLOT_ID
+        dsbi = sbi if same_tables else dsbi.clone()
+        if not same_tables:
+            dsbi[who] = PAD_SLOT_ID
+    state = _normal((slots, heads, headdim, dstate), 0.1, state_dtype, g, device)
+    x = _normal((rows, heads, headdim), 1.0, io_dtype, g, device)
+    dt_shape = (rows, heads, headdim) if dt_per_dim else (rows, heads)
+    dt = _normal(dt_shape, 1.0, torch.float32, g, device)
+    A, D, dt_bias = _head_params(heads, g, device)
+    B = _normal((rows, groups, dstate), 1.0, io_dtype, g, device)
+    C = _normal((rows, groups, dstate), 1.0, io_dtype, g, device)
+    z = _normal((rows, heads, headdim), 1.0, io_dtype, g, device) if with_z else None
+    case = SSUCase(kind="varlen", name=name, state=state, x=x, dt=dt, A=A, B=B, C=C, D=D,
+                   dt_bias=dt_bias, z=z, state_batch_indices=sbi.to(index_dtype),
+                   dst_state_batch_indices=None if same_tables else dsbi.to(index_dtype),
+                   cu_seqlens=None if dense else cu.to(meta_dtype),
+                   num_accepted_tokens=na.to(meta_dtype), dense_steps=fixed_len or 1,
+                   nseqs=nseqs, disable_state_update=disable_state_update)
+    if dense and fixed_len is None:
+        raise ValueError("a dense call needs fixed_len")
+    if with_trackers:
+        case.ring_start = torch.randint(0, ring_buffer_len, (slots,), generator=g, device=device,
+                                        dtype=torch.int64).to(torch.int32)
+        case.prev_num_accepted = torch.randint(0, logical_window + 1, (slots,), generator=g,
+                                               device=device, dtype=torch.int64).to(torch.int32)
+        case.prev_query_len = torch.randint(0, max_len + 1, (slots,), generator=g, device=device,
+                                            dtype=torch.int64).to(torch.int32)
+        case.logical_window = logical_window
+        case.ring_buffer_len = ring_buffer_len
+    return case
+
+
+# ---------------------------------------------------------------------------
+# the named serving workloads
+# ---------------------------------------------------------------------------
+
+def tiny(seed=0, device="cpu", dt_per_dim=False) -> SSUCase:
+    """Tiny single-token decode: batch 4, 8 heads, headdim 64, dstate 16, 1 group,
+    fp32 state [4, 8, 64, 16], identity slot map, no z."""
+    return single_token_case(batch=4, heads=8, headdim=64, dstate=16, groups=1, slots=4,
+                             state_dtype=torch.float32, with_z=False, dt_per_dim=dt_per_dim,
+                             identity_slots=True, seed=seed, device=device, name="tiny")
+
+
+def mamba2_2p7b_decode(seed=0, device="cpu") -> SSUCase:
+    """Mamba2-2.7B-shaped decode: batch 256, 80 heads, headdim 64, dstate 128,
+    1 group, fp32 state pool of 512 slots; int32 slot vector = a random subset
+    with 5% (13) of its entries set to the pad id; z gating on."""
+    return single_token_case(batch=256, heads=80, headdim=64, dstate=128, groups=1, slots=512,
+                             state_dtype=torch.float32, pad_frac=0.05, seed=seed, device=device,
+                             name="mamba2-2.7b-decode-b256")
+
+
+def hybrid_grouped_decode(seed=0, device="cpu") -> SSUCase:
+    """Hybrid-model decode: batch 1024, 128 heads, headdim 64, dstate 128,
+    8 groups (16 heads per group), bf16 state pool of 2048 slots, z on."""
+    return single_token_case(batch=1024, heads=128, headdim=64, dstate=128, groups=8,
+                             slots=2048, state_dtype=torch.bfloat16, seed=seed, device=device,
+                             name="hybrid-grouped-decode-b1024")
+
+
+def mtp_varlen(seed=0, device="cpu") -> SSUCase:
+    """Packed varlen MTP decode: 128 sequences of U{1..4} rows (int32
+    cu_seqlens), 80 heads, headdim 64, dstate 128, 1 group, fp32 state pool of
+    1024; acceptance counts U{1..len}; read and write tables [128, 4] int32 of
+    distinct slots; ReplaySSM trackers int32 [1024] with window 4, ring 8."""
+    return varlen_case(nseqs=128, max_len=4, heads=80, headdim=64, dstate=128, groups=1,
+                       slots=1024, state_dtype=torch.float32, with_trackers=True,
+                       logical_window=4, ring_buffer_len=8, seed=seed, device=device,
+                       name="mtp-varlen-s128")
+
+
+def sweep_case(batch, state_dtype, mode, disable_state_update=False, seed=0,
+               device="cpu") -> SSUCase:
+    """Large-batch sweep point: 128 heads, headdim 64, dstate 128, 8 groups,
+    int64 slot tables with 2% pad sequences, z on.  mode "single": pool 2*batch;
+    mode "mtp": dense 4-step call, one [batch, 4] read/write table of distinct
+    slots (pool 4*batch, the smallest that holds four write slots per sequence)."""
+    name = f"sweep-{mode}-{str(state_dtype).split('.')[-1]}-b{batch}"
+    if disable_state_update:
+        name += "-nowrite"
+    if mode == "single":
+        return single_token_case(batch=batch, heads=128, headdim=64, dstate=128, groups=8,
+                                 slots=2 * batch, state_dtype=state_dtype, pad_frac=0.02,
+                                 index_dtype=torch.int64,
+                                 disable_state_update=disable_state_update, seed=seed,
+                                 device=device, name=name)
+    if mode == "mtp":
+        return varlen_case(nseqs=batch, max_len=4, fixed_len=4, heads=128, headdim=64,
+                           dstate=128, groups=8, slots=4 * batch, state_dtype=state_dtype,
+                           pad_frac=0.02, index_dtype=torch.int64, meta_dtype=torch.int64,
+                           same_tables=True, dense=True,
+                           disable_state_update=disable_state_update, seed=seed,
+                           device=device, name=name)
+    raise ValueError(mode)
+
+
+WORKLOADS = {
+    "tiny": tiny,
+    "mamba2-2.7b-decode": mamba2_2p7b_decode,
+    "hybrid-grouped-decode": hybrid_grouped_decode,
+    "mtp-varlen": mtp_varlen,
+}
