@@ -1,0 +1,256 @@
+/*
+ * ssu.h -- C ABI of the GB300 (sm_103a) Mamba2 selective-state-update decode
+ * library (libssu_gb300.so).
+ *
+ * The operation is the Mamba2 decode step the following pages call
+ * selective_state_update:
+ *   - "vllm.model_executor.layers.mamba.ops.ssu_dispatch" (vLLM API docs and
+ *     ssu_dispatch.py): the unified selective_state_update signature (state,
+ *     x, dt, A, B, C, D, dt_bias, z, dt_softplus, state_batch_indices,
+ *     dst_state_batch_indices, null_block_id, out, num_accepted_tokens,
+ *     cu_seqlens) and the ReplaySSM tracker kernels
+ *     _update_replayssm_ring_trackers_kernel /
+ *     _commit_replayssm_ring_trackers_kernel with their wrappers
+ *     update_/reset_/commit_replayssm_ring_trackers.
+ *   - "mate.mamba" (MATE module source): the FlashInfer-shaped contract of
+ *     selective_state_update -- supported dtypes and layouts, per-head A/D/
+ *     dt_bias (_per_head), one-token route (ssu_one_token, _slot_vector),
+ *     packed varlen route (_packed_selective_state_update, _slot_table,
+ *     _dense_seq_starts), pad_slot_id and disable_state_update.
+ * For every sequence and head, with g = head / (nheads / ngroups):
+ *   dt' = dt + dt_bias; dt' = softplus(dt') if dt_softplus; dA = exp(A * dt')
+ *   h[p][n] <- h[p][n] * dA + dt' * x[p] * B[g][n]
+ *   y[p] = sum_n h[p][n] * C[g][n] + D * x[p];  y *= silu(z[p]) if z given
+ * computed in fp32 registers; the state is read once from its slot and the
+ * new state (rounded to nearest even in the state dtype) written to the
+ * destination slot(s).
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates nothing, never synchronises, never copies device data to the
+ *     host, and issues at most one kernel launch on `stream` (a
+ *     cudaStream_t; NULL is the legacy default stream).
+ *   - Arguments are validated on the host before any launch; a rejected call
+ *     launches nothing and changes nothing.  SSU_ERR_INVALID_ARGUMENT mirrors
+ *     the pages' ValueError cases, SSU_ERR_UNSUPPORTED their
+ *     NotImplementedError cases, SSU_ERR_CUDA a failed launch.
+ *     ssu_last_error() gives a message for the calling thread's last failure.
+ *   - Slot indices are int32 or int64.  An index equal to pad_slot_id, or
+ *     outside [0, slots), is skipped on the device (no read, no write; the
+ *     pages' tracker kernels mask the same way); it never faults.
+ *   - A call with zero sequences returns SSU_OK without launching.
+ *   - Calls that write the same state slot from two sequences race (the
+ *     result is undefined), as in the pages' kernels.
+ */
+#ifndef SSU_GB300_H
+#define SSU_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t */
+
+typedef enum ssu_status {
+  SSU_OK = 0,
+  SSU_ERR_INVALID_ARGUMENT = 1, /* shapes, strides, dtypes or values the contract rejects */
+  SSU_ERR_UNSUPPORTED = 2,      /* a valid request this build does not implement */
+  SSU_ERR_CUDA = 3              /* the kernel launch failed */
+} ssu_status;
+
+typedef enum ssu_dtype {
+  SSU_F32 = 0,
+  SSU_BF16 = 1,
+  SSU_F16 = 2,
+  SSU_I32 = 3,
+  SSU_I64 = 4
+} ssu_dtype;
+
+/*
+ * Operands of one selective-state-update call (both routes).  Strides are in
+ * ELEMENTS.  Rows are packed tokens: the one-token route has one row per
+ * sequence, the varlen route `rows` rows split by cu_seqlens.
+ *
+ * state      [slots, nheads, headdim, dstate], contiguous, 16-byte aligned,
+ *            F32 / BF16 / F16 ("mate.mamba": state fp16/bf16/fp32,
+ *            contiguous).  Read and written in place.
+ * io_dtype   BF16 or F16: the dtype of x, z, B and C.
+ * x          [rows, nheads, headdim]: element (r, h, p) at
+ *            x[r * x_row_stride + h * x_head_stride + p].
+ * z          same layout as x, or NULL (no silu gate).
+ * out        y, same layout as x with its own strides; out_dtype is io_dtype
+ *            (the contract) or F32 (full-precision output, an extension of
+ *            this library).  Written for every row a sequence covers.
+ * dt         fp32, element (r, h, p) at
+ *            dt[r * dt_row_stride + h * dt_head_stride + p * dt_dim_stride];
+ *            dt_dim_stride = 0 is the per-head form [rows, nheads(, 1)].
+ * B, C       [rows, ngroups, dstate], io_dtype: element (r, g, n) at
+ *            B[r * B_row_stride + g * B_group_stride + n].
+ * A, D, dt_bias  fp32 per head: A[h * A_stride]; D and dt_bias may be NULL
+ *            (treated as 0).  A stride of 0 ties every head to one value.
+ * dt_softplus, disable_state_update: flags (0 / 1).
+ * pad_slot_id: slot id that marks a padded entry (vLLM passes its null
+ *            block id; "mate.mamba" defaults to -1).
+ */
+typedef struct ssu_params {
+  void* state;
+  ssu_dtype state_dtype;
+  int64_t slots, nheads, headdim, dstate, ngroups;
+  ssu_dtype io_dtype;
+  const void* x;
+  int64_t x_row_stride, x_head_stride;
+  const void* z;
+  int64_t z_row_stride, z_head_stride;
+  void* out;
+  ssu_dtype out_dtype;
+  int64_t out_row_stride, out_head_stride;
+  const float* dt;
+  int64_t dt_row_stride, dt_head_stride, dt_dim_stride;
+  const void* B;
+  int64_t B_row_stride, B_group_stride;
+  const void* C;
+  int64_t C_row_stride, C_group_stride;
+  const float* A;
+  int64_t A_stride;
+  const float* D;
+  int64_t D_stride;
+  const float* dt_bias;
+  int64_t dt_bias_stride;
+  int dt_softplus;
+  int disable_state_update;
+  int64_t pad_slot_id;
+} ssu_params;
+
+/*
+ * A slot table of the packed route ("mate.mamba", _slot_table): entry
+ * (sequence s, position t) is indices[s * seq_stride + t * step_stride].  A
+ * flat [rows] table has strides (1, 1); a [sequences, steps] table
+ * (steps, 1).  Positions t >= steps, or entries at or beyond numel, do not
+ * exist (treated like a pad entry).  indices == NULL means "no table".
+ */
+typedef struct ssu_slot_table {
+  const void* indices;
+  int64_t numel;
+  int64_t seq_stride, step_stride;
+  int64_t steps;
+} ssu_slot_table;
+
+/*
+ * One-token decode: sequence b is row b of x/dt/B/C/z/out, b in [0, batch).
+ * ("mate.mamba": ssu_one_token route and _slot_vector; "ssu_dispatch":
+ * selective_state_update without cu_seqlens.)
+ *   state_batch_indices      [batch] read slots, or NULL for slot b
+ *                            (then batch must not exceed slots).
+ *   dst_state_batch_indices  [batch] write slots, or NULL to write back to
+ *                            the read slot (in place).
+ *   index_dtype              SSU_I32 or SSU_I64 for both tables.
+ * A sequence whose read slot is pad / out of range runs from a zero state and
+ * writes no state; y is still produced.  A pad / out-of-range write slot
+ * skips only that write.  disable_state_update writes no state at all.
+ */
+ssu_status ssu_update(const ssu_params* p, int64_t batch,
+                      const void* state_batch_indices,
+                      const void* dst_state_batch_indices,
+                      ssu_dtype index_dtype,
+                      struct CUstream_st* stream);
+
+/*
+ * Packed variable-length / speculative (MTP) update.  ("mate.mamba":
+ * ssu_packed_varlen route, _packed_selective_state_update, dense 4-D
+ * folding via _dense_seq_starts; "ssu_dispatch": selective_state_update with
+ * cu_seqlens and num_accepted_tokens.)
+ *   nseqs, rows          sequences and packed rows of this call.
+ *   cu_seqlens           [nseqs + 1] row starts (int, meta_dtype); sequence s
+ *                        owns rows [cu[s], cu[s+1]).  NULL: the dense form,
+ *                        every sequence owns `dense_steps` consecutive rows
+ *                        (rows must equal nseqs * dense_steps).
+ *   num_accepted_tokens  [nseqs] (meta_dtype) or NULL.  Sequence s reads its
+ *                        state from position num_accepted[s] - 1 of `src`
+ *                        (position 0 when NULL).  Requires a src table.
+ *   meta_dtype           SSU_I32 / SSU_I64 for cu_seqlens and
+ *                        num_accepted_tokens (they share it, as the pages
+ *                        require).
+ *   src                  read table, or NULL / indices NULL: sequence s reads
+ *                        slot s (then nseqs must not exceed slots).
+ *   dst                  write table: step t of sequence s writes position t.
+ *                        NULL / indices NULL: the read table's position t
+ *                        (or slot s when there is no read table either).
+ *   index_dtype          SSU_I32 / SSU_I64 for both tables.
+ * The chain over a sequence's rows stays in fp32 registers; each step's state
+ * is rounded only when it is written to its destination slot.  An empty
+ * sequence reads and writes nothing.  A read position outside the table, or a
+ * pad / out-of-range read slot, runs from a zero state and writes no state.
+ * Row ranges are clamped to [0, rows).
+ */
+ssu_status ssu_update_varlen(const ssu_params* p, int64_t nseqs, int64_t rows,
+                             const void* cu_seqlens, int64_t dense_steps,
+                             const void* num_accepted_tokens, ssu_dtype meta_dtype,
+                             const ssu_slot_table* src, const ssu_slot_table* dst,
+                             ssu_dtype index_dtype,
+                             struct CUstream_st* stream);
+
+/*
+ * ReplaySSM ring-tracker update or reset ("ssu_dispatch":
+ * _update_replayssm_ring_trackers_kernel, update_replayssm_ring_trackers,
+ * reset_replayssm_ring_trackers).  Trackers are int32 vectors indexed by
+ * slot; num_states is the shortest of the three lengths.  Sequence i's slot
+ * is state_batch_indices[i * sbi_stride] (pass the row length of a 2-D
+ * table to use its column 0).
+ *   reset != 0: zero all three trackers of every valid slot
+ *               (logical_window / ring_buffer_len are ignored).
+ *   reset == 0: with prev = prev_num_accepted[slot], start = ring_start[slot]:
+ *               if prev + 1 > logical_window:
+ *                   ring_start = (start + prev) % ring_buffer_len; prev = 1
+ *               else prev = prev + 1.   prev_query_len is left unchanged.
+ * int32 arithmetic wraps; % truncates toward zero.  ring_buffer_len must be
+ * >= 1 when reset == 0.
+ */
+ssu_status ssu_ring_update(int32_t* ring_start, int64_t ring_start_len,
+                           int32_t* prev_num_accepted, int64_t prev_num_accepted_len,
+                           int32_t* prev_query_len, int64_t prev_query_len_len,
+                           const void* state_batch_indices, int64_t sbi_stride,
+                           ssu_dtype index_dtype, int64_t nseqs, int reset,
+                           int32_t logical_window, int32_t ring_buffer_len,
+                           int64_t pad_slot_id, struct CUstream_st* stream);
+
+/*
+ * ReplaySSM ring-tracker commit of the previous speculative window
+ * ("ssu_dispatch": _commit_replayssm_ring_trackers_kernel,
+ * commit_replayssm_ring_trackers).  Slots as in ssu_ring_update.  For a
+ * valid slot of sequence i, with acc = prev_num_accepted[slot],
+ * start = ring_start[slot], pql = prev_query_len[slot],
+ * a = num_accepted_tokens[i]:
+ *   must = pql > 0 && acc + pql > logical_window
+ *   ring_start        = must ? (start + acc) % ring_buffer_len : start
+ *   prev_num_accepted = pql == 0 ? 0 : (must ? a : acc + a)
+ *   prev_query_len    = query_start_loc[i + 1] - query_start_loc[i]
+ * num_accepted_tokens [nseqs] and query_start_loc [nseqs + 1] are meta_dtype
+ * (I32 / I64); stored values wrap to int32.  ring_buffer_len must be >= 1.
+ */
+ssu_status ssu_ring_commit(int32_t* ring_start, int64_t ring_start_len,
+                           int32_t* prev_num_accepted, int64_t prev_num_accepted_len,
+                           int32_t* prev_query_len, int64_t prev_query_len_len,
+                           const void* state_batch_indices, int64_t sbi_stride,
+                           ssu_dtype index_dtype,
+                           const void* num_accepted_tokens, const void* query_start_loc,
+                           ssu_dtype meta_dtype, int64_t nseqs,
+                           int32_t logical_window, int32_t ring_buffer_len,
+                           int64_t pad_slot_id, struct CUstream_st* stream);
+
+/* Static description of a status code. */
+const char* ssu_status_string(ssu_status status);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* ssu_last_error(void);
+
+/* ABI version of this header (bumped on any incompatible change). */
+#define SSU_ABI_VERSION 1
+int ssu_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSU_GB300_H */

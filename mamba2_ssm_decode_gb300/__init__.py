@@ -1,0 +1,14 @@
+"""GB300 (sm_103a) Mamba2 selective-state-update decode.
+
+The C ABI lives in include/ssu.h and libssu_gb300.so (built in-tree by
+``mamba2_ssm_decode_gb300.build``); this package binds it for CUDA torch
+tensors:
+
+  ssu_update         one-token decode step
+  ssu_update_varlen  packed variable-length / speculative (MTP) step
+  ssu_ring_update    ReplaySSM ring-tracker update or reset
+  ssu_ring_commit    ReplaySSM ring-tracker commit of the previous window
+"""
+from .api import ssu_ring_commit, ssu_ring_update, ssu_update, ssu_update_varlen
+
+__all__ = ["ssu_update", "ssu_update_varlen", "ssu_ring_update", "ssu_ring_commit"]

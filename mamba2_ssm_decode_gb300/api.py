@@ -1,0 +1,330 @@
+"""Python binding of the C ABI (include/ssu.h): argument marshalling only.
+
+Each function takes CUDA torch tensors, checks that they describe the layout
+the ABI expects (no hidden copies, no compute), and calls the library on the
+current torch stream of the tensors' device.  Every step of the operation runs
+in libssu_gb300.so; there is no CPU or torch fallback.
+
+Exceptions follow the pages' conventions ("mate.mamba"): ValueError for a
+rejected argument, NotImplementedError for a capability this build does not
+implement, RuntimeError for a failed launch.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+
+_FLOAT_DT = {torch.float32: _abi.SSU_F32, torch.bfloat16: _abi.SSU_BF16,
+             torch.float16: _abi.SSU_F16}
+_INT_DT = {torch.int32: _abi.SSU_I32, torch.int64: _abi.SSU_I64}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require_cuda(*tensors):
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("libssu_gb300 works on CUDA tensors only (there is no CPU path)")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"all tensors must be on one device, got {dev} and {t.device}")
+    return dev
+
+
+def _float_dtype(t, name):
+    if t.dtype not in _FLOAT_DT:
+        raise NotImplementedError(f"{name} dtype {t.dtype} is not supported")
+    return _FLOAT_DT[t.dtype]
+
+
+def _int_dtype(t, name):
+    if t.dtype not in _INT_DT:
+        raise ValueError(f"{name} must be int32 or int64, got {t.dtype}")
+    return _INT_DT[t.dtype]
+
+
+def _rows3(t, name, rows, heads, dim):
+    """(row stride, head stride) of a [rows, heads, dim] operand with unit dim stride."""
+    if t.dim() != 3 or tuple(t.shape) != (rows, heads, dim):
+        raise ValueError(f"{name} must be [{rows}, {heads}, {dim}], got {tuple(t.shape)}")
+    if dim > 1 and t.stride(2) != 1:
+        raise ValueError(f"{name} must be contiguous along dim (stride 1), got {t.stride()}")
+    return t.stride(0), t.stride(1)
+
+
+def _per_head(t, heads, name):
+    """Stride of a per-head fp32 parameter: [H], [H, 1], or a tied [H, dim, dstate]
+    view with zero inner strides ("mate.mamba", _per_head)."""
+    if t is None:
+        return 0
+    if t.dtype != torch.float32:
+        raise NotImplementedError(f"{name} must be fp32, got {t.dtype}")
+    if t.shape[0] != heads:
+        raise ValueError(f"{name} must have one entry per head ({heads}), got {tuple(t.shape)}")
+    if t.dim() == 1:
+        return t.stride(0)
+    if t.dim() == 2 and t.shape[1] == 1:
+        return t.stride(0)
+    if t.dim() == 3 and t.stride(1) == 0 and t.stride(2) == 0:
+        return t.stride(0)
+    raise NotImplementedError(
+        f"{name}: only per-head (tied) values are implemented; got shape {tuple(t.shape)} "
+        f"with strides {t.stride()}")
+
+
+def _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
+            disable_state_update, rows):
+    if state.dim() != 4:
+        raise ValueError(f"state must be [slots, heads, dim, dstate], got {tuple(state.shape)}")
+    if not state.is_contiguous():
+        raise ValueError("state must be contiguous")
+    slots, H, P, N = state.shape
+    sdt = _float_dtype(state, "state")
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise NotImplementedError(f"x must be bf16 or fp16, got {x.dtype}")
+    io = _FLOAT_DT[x.dtype]
+    xs = _rows3(x, "x", rows, H, P)
+    zs = (0, 0) if z is None else _rows3(z, "z", rows, H, P)
+    if z is not None and z.dtype != x.dtype:
+        raise ValueError("z must match x in shape and dtype")
+    os_ = _rows3(out, "out", rows, H, P)
+    if out.dtype not in (x.dtype, torch.float32):
+        raise ValueError(f"out must be {x.dtype} (or fp32), got {out.dtype}")
+    if dt.dtype != torch.float32:
+        raise NotImplementedError(f"dt must be fp32, got {dt.dtype}")
+    if dt.dim() == 2 and tuple(dt.shape) == (rows, H):
+        dts = (dt.stride(0), dt.stride(1), 0)
+    elif dt.dim() == 3 and tuple(dt.shape[:2]) == (rows, H) and dt.shape[2] in (1, P):
+        dts = (dt.stride(0), dt.stride(1), 0 if dt.shape[2] == 1 else dt.stride(2))
+    else:
+        raise ValueError(f"dt must be [{rows}, {H}], [{rows}, {H}, 1] or [{rows}, {H}, {P}], "
+                         f"got {tuple(dt.shape)}")
+    if B.dim() != 3 or C.shape != B.shape or B.shape[0] != rows or B.shape[2] != N:
+        raise ValueError(f"B/C must be [rows, groups, dstate]; got B={tuple(B.shape)}, "
+                         f"C={tuple(C.shape)}")
+    if B.dtype != x.dtype or C.dtype != x.dtype:
+        raise ValueError("B and C must share the x dtype")
+    if (N > 1 and (B.stride(2) != 1 or C.stride(2) != 1)):
+        raise ValueError("B and C must be contiguous along dstate")
+    G = B.shape[1]
+    p = _abi.SSUParams()
+    p.state, p.state_dtype = state.data_ptr(), sdt
+    p.slots, p.nheads, p.headdim, p.dstate, p.ngroups = slots, H, P, N, G
+    p.io_dtype = io
+    p.x, (p.x_row_stride, p.x_head_stride) = x.data_ptr(), xs
+    p.z, (p.z_row_stride, p.z_head_stride) = (z.data_ptr() if z is not None else None), zs
+    p.out, p.out_dtype = out.data_ptr(), _FLOAT_DT[out.dtype]
+    p.out_row_stride, p.out_head_stride = os_
+    p.dt = dt.data_ptr()
+    p.dt_row_stride, p.dt_head_stride, p.dt_dim_stride = dts
+    p.B, p.B_row_stride, p.B_group_stride = B.data_ptr(), B.stride(0), B.stride(1)
+    p.C, p.C_row_stride, p.C_group_stride = C.data_ptr(), C.stride(0), C.stride(1)
+    p.A, p.A_stride = A.data_ptr(), _per_head(A, H, "A")
+    p.D, p.D_stride = (D.data_ptr() if D is not None else None), _per_head(D, H, "D")
+    p.dt_bias = dt_bias.data_ptr() if dt_bias is not None else None
+    p.dt_bias_stride = _per_head(dt_bias, H, "dt_bias")
+    p.dt_softplus = int(bool(dt_softplus))
+    p.disable_state_update = int(bool(disable_state_update))
+    p.pad_slot_id = int(pad_slot_id)
+    return p
+
+
+def ssu_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
+               state_batch_indices=None, dst_state_batch_indices=None, pad_slot_id=-1,
+               out=None, disable_state_update=False, out_dtype=None, stream=None):
+    """One-token selective state update (C ABI ``ssu_update``).
+
+    state [slots, H, P, N] (updated in place); x, z [batch, H, P]; dt [batch, H]
+    or [batch, H, P] fp32; B, C [batch, G, N]; A, D, dt_bias per head fp32;
+    slot vectors [batch] int32/int64.  Returns ``out`` [batch, H, P] (x dtype,
+    or ``out_dtype=torch.float32``)."""
+    dev = _require_cuda(state, x, dt, A, B, C, D, z, dt_bias, state_batch_indices,
+                        dst_state_batch_indices, out)
+    batch = x.shape[0]
+    if out is None:
+        out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=dev)
+    p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
+                disable_state_update, batch)
+    idx_dt = 0
+    for name, t in (("state_batch_indices", state_batch_indices),
+                    ("dst_state_batch_indices", dst_state_batch_indices)):
+        if t is not None:
+            if t.dim() != 1 or t.shape[0] != batch:
+                raise ValueError(f"{name} must be [sequences] ({batch}) on the one-token path; "
+                                 f"got {tuple(t.shape)}")
+            if t.stride(0) != 1 and batch > 1:
+                raise ValueError(f"{name} must be contiguous")
+            d = _int_dtype(t, name)
+            if idx_dt and d != idx_dt:
+                raise ValueError("state_batch_indices and dst_state_batch_indices must share a dtype")
+            idx_dt = d
+    _abi.check(_abi.lib().ssu_update(
+        ctypes.byref(p), batch, _ptr(state_batch_indices), _ptr(dst_state_batch_indices),
+        idx_dt or _abi.SSU_I32, _stream(dev, stream)))
+    return out
+
+
+def _table(t, name):
+    if t is None:
+        return _abi.SlotTable(None, 0, 0, 0, 0), 0
+    d = _int_dtype(t, name)
+    if t.dim() == 1:   # flat [rows]: entry (s, t) = s + t ("mate.mamba", _slot_table)
+        return _abi.SlotTable(t.data_ptr(), t.numel(), t.stride(0), t.stride(0), t.numel()), d
+    if t.dim() == 2:   # [sequences, steps]
+        numel = (t.shape[0] - 1) * t.stride(0) + (t.shape[1] - 1) * t.stride(1) + 1
+        return _abi.SlotTable(t.data_ptr(), numel if t.numel() else 0, t.stride(0), t.stride(1),
+                              t.shape[1]), d
+    raise ValueError(f"{name} must be the flat [rows] or the 2-D [sequences, steps] slot "
+                     f"table; got {tuple(t.shape)}")
+
+
+def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
+                      cu_seqlens=None, num_accepted_tokens=None, state_batch_indices=None,
+                      dst_state_batch_indices=None, pad_slot_id=-1, out=None,
+                      disable_state_update=False, nseqs=None, out_dtype=None, stream=None):
+    """Packed varlen / MTP selective state update (C ABI ``ssu_update_varlen``).
+
+    x is packed [rows, H, P] with ``cu_seqlens`` [S + 1], or dense
+    [batch, steps, H, P] (then dt/B/C/z are 4-D as well and equal-length
+    sequences are implied).  Slot tables are [S, T] or flat [rows];
+    ``num_accepted_tokens`` [S] picks the read position (count - 1)."""
+    dev = _require_cuda(state, x, dt, A, B, C, D, z, dt_bias, cu_seqlens, num_accepted_tokens,
+                        state_batch_indices, dst_state_batch_indices, out)
+    dense_steps = 1
+    dense_out = None
+    if x.dim() == 4:
+        batch, steps = x.shape[:2]
+        rows = batch * steps
+
+        def flat(t, name):
+            if t is None:
+                return None
+            if t.dim() != 4:
+                raise ValueError(f"a dense (4-D) x requires a 4-D {name} as well, got "
+                                 f"{tuple(t.shape)}")
+            return t.view(rows, *t.shape[2:])  # a view, never a copy
+
+        x, dt, B, C, z = flat(x, "x"), flat(dt, "dt"), flat(B, "B"), flat(C, "C"), flat(z, "z")
+        if out is not None:
+            dense_out = out
+            out = out.view(rows, *out.shape[2:])
+        if cu_seqlens is None:
+            dense_steps = steps
+            nseqs = batch
+    rows = x.shape[0]
+    if nseqs is None:
+        if cu_seqlens is not None:
+            nseqs = cu_seqlens.numel() - 1
+        elif num_accepted_tokens is not None:
+            nseqs = num_accepted_tokens.numel()
+        elif state_batch_indices is not None:
+            nseqs = state_batch_indices.shape[0]
+        elif dst_state_batch_indices is not None:
+            nseqs = dst_state_batch_indices.shape[0]
+        else:
+            raise ValueError("a packed multi-token call must carry per-sequence metadata: "
+                             "state_batch_indices, dst_state_batch_indices, "
+                             "num_accepted_tokens or cu_seqlens")
+    if out is None:
+        out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=dev)
+    p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
+                disable_state_update, rows)
+    meta_dt = 0
+    if cu_seqlens is not None:
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() != nseqs + 1:
+            raise ValueError(f"cu_seqlens must hold {nseqs + 1} entries, got "
+                             f"{tuple(cu_seqlens.shape)}")
+        if cu_seqlens.stride(0) != 1 and cu_seqlens.numel() > 1:
+            raise ValueError("cu_seqlens must be contiguous")
+        meta_dt = _int_dtype(cu_seqlens, "cu_seqlens")
+    if num_accepted_tokens is not None:
+        if num_accepted_tokens.dim() != 1 or num_accepted_tokens.numel() != nseqs:
+            raise ValueError(f"num_accepted_tokens must be [sequences] ({nseqs}), got "
+                             f"{tuple(num_accepted_tokens.shape)}")
+        if num_accepted_tokens.stride(0) != 1 and nseqs > 1:
+            raise ValueError("num_accepted_tokens must be contiguous")
+        d = _int_dtype(num_accepted_tokens, "num_accepted_tokens")
+        if meta_dt and d != meta_dt:
+            raise ValueError("cu_seqlens and num_accepted_tokens must share a dtype")
+        meta_dt = d
+    src, sd = _table(state_batch_indices, "state_batch_indices")
+    dst, dd = _table(dst_state_batch_indices, "dst_state_batch_indices")
+    if sd and dd and sd != dd:
+        raise ValueError("state_batch_indices and dst_state_batch_indices must share a dtype")
+    _abi.check(_abi.lib().ssu_update_varlen(
+        ctypes.byref(p), nseqs, rows, _ptr(cu_seqlens), dense_steps, _ptr(num_accepted_tokens),
+        meta_dt or _abi.SSU_I32, ctypes.byref(src), ctypes.byref(dst), sd or dd or _abi.SSU_I32,
+        _stream(dev, stream)))
+    return dense_out if dense_out is not None else out
+
+
+def _tracker_args(ring_start, prev_num_accepted, prev_query_len, state_batch_indices):
+    for name, t in (("ring_start", ring_start), ("prev_num_accepted", prev_num_accepted),
+                    ("prev_query_len", prev_query_len)):
+        if t.dtype != torch.int32:
+            raise NotImplementedError(f"{name} must be int32, got {t.dtype}")
+        if t.dim() != 1 or (t.numel() > 1 and t.stride(0) != 1):
+            raise ValueError(f"{name} must be a contiguous vector")
+    sbi = state_batch_indices
+    if sbi.dim() > 2:
+        raise ValueError(f"state_batch_indices must be [S] or [S, T], got {tuple(sbi.shape)}")
+    nseqs = sbi.shape[0]
+    stride = sbi.stride(0)   # column 0 of a 2-D table
+    return nseqs, stride, _int_dtype(sbi, "state_batch_indices")
+
+
+def ssu_ring_update(ring_start, prev_num_accepted, prev_query_len, state_batch_indices,
+                    logical_window=None, ring_buffer_len=None, pad_slot_id=-1, stream=None):
+    """ReplaySSM tracker update (C ABI ``ssu_ring_update``); ``logical_window=None``
+    resets the trackers of the given slots, as the pages' wrapper does."""
+    dev = _require_cuda(ring_start, prev_num_accepted, prev_query_len, state_batch_indices)
+    nseqs, stride, idt = _tracker_args(ring_start, prev_num_accepted, prev_query_len,
+                                       state_batch_indices)
+    reset = logical_window is None
+    if not reset and ring_buffer_len is None:
+        raise ValueError("ring_buffer_len is required when logical_window is given")
+    _abi.check(_abi.lib().ssu_ring_update(
+        _ptr(ring_start), ring_start.numel(), _ptr(prev_num_accepted), prev_num_accepted.numel(),
+        _ptr(prev_query_len), prev_query_len.numel(), _ptr(state_batch_indices), stride, idt,
+        nseqs, int(reset), 0 if reset else int(logical_window),
+        1 if reset else int(ring_buffer_len), int(pad_slot_id), _stream(dev, stream)))
+
+
+def ssu_ring_commit(ring_start, prev_num_accepted, prev_query_len, state_batch_indices,
+                    num_accepted_tokens, query_start_loc, logical_window, ring_buffer_len,
+                    pad_slot_id=-1, stream=None):
+    """ReplaySSM tracker commit (C ABI ``ssu_ring_commit``)."""
+    dev = _require_cuda(ring_start, prev_num_accepted, prev_query_len, state_batch_indices,
+                        num_accepted_tokens, query_start_loc)
+    nseqs, stride, idt = _tracker_args(ring_start, prev_num_accepted, prev_query_len,
+                                       state_batch_indices)
+    if num_accepted_tokens.numel() < nseqs or query_start_loc.numel() < nseqs + 1:
+        raise ValueError("num_accepted_tokens needs one entry and query_start_loc one start "
+                         "per sequence (plus the total)")
+    mdt = _int_dtype(num_accepted_tokens, "num_accepted_tokens")
+    if _int_dtype(query_start_loc, "query_start_loc") != mdt:
+        raise ValueError("num_accepted_tokens and query_start_loc must share a dtype")
+    for name, t in (("num_accepted_tokens", num_accepted_tokens),
+                    ("query_start_loc", query_start_loc)):
+        if t.dim() != 1 or (t.numel() > 1 and t.stride(0) != 1):
+            raise ValueError(f"{name} must be a contiguous vector")
+    _abi.check(_abi.lib().ssu_ring_commit(
+        _ptr(ring_start), ring_start.numel(), _ptr(prev_num_accepted), prev_num_accepted.numel(),
+        _ptr(prev_query_len), prev_query_len.numel(), _ptr(state_batch_indices), stride, idt,
+        _ptr(num_accepted_tokens), _ptr(query_start_loc), mdt, nseqs, int(logical_window),
+        int(ring_buffer_len), int(pad_slot_id), _stream(dev, stream)))

@@ -1,0 +1,473 @@
+// ssu_kernel.cuh -- sm_103a kernels of the Mamba2 selective state update.
+//
+// The operation ("vllm.model_executor.layers.mamba.ops.ssu_dispatch":
+// selective_state_update; "mate.mamba": ssu_one_token / ssu_packed_varlen):
+// for one (sequence, head) the state block h[P][N] is read from its slot,
+// advanced through the sequence's rows
+//     h[p][n] <- h[p][n] * exp(A dt'_p) + dt'_p x[p] B[n]
+//     y[p]     = sum_n h[p][n] C[n] + D x[p]   (times silu(z[p]))
+// and written to each row's destination slot.
+//
+// Design (HBM-bound; about 6 flops per state element per token, far below
+// the fp32 ridge, so no tensor cores):
+//   * One CTA owns ROWS consecutive rows (headdim positions) of one head of
+//     one sequence: grid = sequences x heads x row tiles, the tile index
+//     fastest so consecutive CTAs stream one slot's contiguous blocks.
+//   * A state row is dstate elements.  LPR lanes share a row and each lane
+//     owns CPL 16-byte chunks of it, interleaved (chunk q + c * LPR) so one
+//     warp load instruction covers RPW rows x 128 contiguous bytes.  Every
+//     thread issues all UNR x CPL 16-byte loads of its rows before it uses
+//     any, so each SM keeps tens of KB of state reads in flight.
+//   * The per-step vectors (B, C of the group, and per row dA, dt' x, D x,
+//     silu(z)) are staged once per CTA in shared memory, in fp32, while the
+//     state loads are in flight; up to LMAX steps are staged at a time.
+//   * The state stays in fp32 registers for the whole chain of a sequence;
+//     y[p] is reduced across the LPR lanes of a row with xor shuffles.
+//   * State loads bypass L1 (read once); stores are plain write-back.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssu {
+
+// ---------------------------------------------------------------------------
+// kernel parameters (normalised on the host from ssu_params)
+// ---------------------------------------------------------------------------
+struct KParams {
+  void* state;
+  int64_t slots;
+  int H, P, hr;  // heads, headdim, heads per group
+  int tiles;     // row tiles per head
+  const void* x;
+  int64_t x_rs, x_hs;
+  const void* z;
+  int64_t z_rs, z_hs;
+  void* out;
+  int64_t o_rs, o_hs;
+  int out_f32;
+  const float* dt;
+  int64_t dt_rs, dt_hs, dt_ds;
+  const void* B;
+  int64_t B_rs, B_gs;
+  const void* C;
+  int64_t C_rs, C_gs;
+  const float* A;
+  int64_t A_s;
+  const float* D;
+  int64_t D_s;
+  const float* dt_bias;
+  int64_t bias_s;
+  int softplus;
+  int disable;
+  int64_t pad;
+};
+
+struct TableArgs {
+  const void* idx;  // nullptr = no table
+  int64_t numel, ss, ts, steps;
+};
+
+struct OneTokenArgs {
+  const void* sbi;   // nullptr = slot b
+  const void* dsbi;  // nullptr = in place
+  int idx64;
+};
+
+struct VarlenArgs {
+  int64_t rows;
+  const void* cu;  // nullptr = dense
+  int64_t dense_steps;
+  const void* na;  // nullptr = position 0
+  int meta64;
+  TableArgs src, dst;
+  int idx64;
+};
+
+// ---------------------------------------------------------------------------
+// element types
+// ---------------------------------------------------------------------------
+template <class T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+  static constexpr int VEC = 4;  // elements per 16-byte chunk
+  __device__ static __forceinline__ void unpack(const uint4& r, float* f) {
+    f[0] = __uint_as_float(r.x);
+    f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z);
+    f[3] = __uint_as_float(r.w);
+  }
+  __device__ static __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int VEC = 8;
+  __device__ static __forceinline__ void unpack(const uint4& r, float* f) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);              // element 2i: low half
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);  // element 2i+1: high half
+    }
+  }
+  __device__ static __forceinline__ uint4 pack(const float* f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 v = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);  // .x low, .y high
+      w[i] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+template <>
+struct Elem<__half> {
+  static constexpr int VEC = 8;
+  __device__ static __forceinline__ void unpack(const uint4& r, float* f) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h2 = *reinterpret_cast<const __half2*>(&w[i]);
+      float2 v = __half22float2(h2);
+      f[2 * i] = v.x;
+      f[2 * i + 1] = v.y;
+    }
+  }
+  __device__ static __forceinline__ uint4 pack(const float* f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 v = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+template <class IT>
+__device__ __forceinline__ float io_to_float(IT v);
+template <>
+__device__ __forceinline__ float io_to_float<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+template <>
+__device__ __forceinline__ float io_to_float<__half>(__half v) {
+  return __half2float(v);
+}
+template <class IT>
+__device__ __forceinline__ IT float_to_io(float v);
+template <>
+__device__ __forceinline__ __nv_bfloat16 float_to_io<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+template <>
+__device__ __forceinline__ __half float_to_io<__half>(float v) {
+  return __float2half_rn(v);
+}
+
+// ---------------------------------------------------------------------------
+// lane layout of one state row
+// ---------------------------------------------------------------------------
+template <class ST, int N>
+struct RowLayout {
+  static constexpr int VEC = Elem<ST>::VEC;
+  static_assert(N % VEC == 0, "dstate must fill whole 16-byte chunks");
+  static constexpr int CHUNKS = N / VEC;                // 16-byte chunks per row
+  static constexpr int LPR = CHUNKS >= 8 ? 8 : CHUNKS;  // lanes sharing one row
+  static constexpr int CPL = CHUNKS / LPR;              // chunks per lane
+  static constexpr int RPW = 32 / LPR;                  // rows per warp instruction
+  static constexpr int EPL = CPL * VEC;                 // elements per lane per row
+  static_assert(CHUNKS % LPR == 0 && 32 % LPR == 0, "unsupported dstate");
+};
+
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int64_t load_int(const void* p, int64_t i, int is64) {
+  return is64 ? static_cast<const int64_t*>(p)[i]
+              : static_cast<int64_t>(static_cast<const int32_t*>(p)[i]);
+}
+
+// entry (seq, pos) of a slot table; false when the table has no such entry
+__device__ __forceinline__ bool table_entry(const TableArgs& t, int64_t seq, int64_t pos,
+                                            int is64, int64_t* out) {
+  if (pos < 0 || pos >= t.steps) return false;
+  const int64_t e = seq * t.ss + pos * t.ts;
+  if (e < 0 || e >= t.numel) return false;
+  *out = load_int(t.idx, e, is64);
+  return true;
+}
+
+__device__ __forceinline__ bool slot_ok(int64_t slot, int64_t pad, int64_t slots) {
+  return slot != pad && slot >= 0 && slot < slots;
+}
+
+__device__ __forceinline__ float softplus_f(float v) {
+  // log(1 + e^v) written as max(v, 0) + log1p(e^-|v|): no overflow, no cutoff
+  return fmaxf(v, 0.0f) + log1pf(expf(-fabsf(v)));
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  return __ldcg(reinterpret_cast<const uint4*>(p));  // L2 only: the state is read once
+}
+
+__device__ __forceinline__ void st_state(void* p, const uint4& v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <class ST, class IT, int N, int WARPS, int UNR, int LMAX>
+struct SSUConfig {
+  using L = RowLayout<ST, N>;
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int ROWS = WARPS * L::RPW * UNR;  // headdim rows per CTA
+};
+
+// Shared-memory staging of up to LMAX steps for one CTA (read with 16-byte
+// vector loads, hence the alignment).
+template <int N, int ROWS, int LMAX>
+struct __align__(16) Stage {
+  float B[LMAX][N];
+  float C[LMAX][N];
+  float dA[LMAX][ROWS];
+  float dtx[LMAX][ROWS];  // dt' * x
+  float Dx[LMAX][ROWS];   // D * x
+  float gate[LMAX][ROWS]; // silu(z), or 1
+};
+
+// Stage steps [t0, t0 + n) of rows [r0 + t0, ...) for head h / group g.
+template <class IT, int N, int ROWS, int LMAX, int THREADS>
+__device__ __forceinline__ void stage_steps(Stage<N, ROWS, LMAX>& s, const KParams& p,
+                                            int64_t r0, int t0, int n, int h, int g, int p0,
+                                            float A, float Dh, float bias) {
+  const IT* Bp = static_cast<const IT*>(p.B);
+  const IT* Cp = static_cast<const IT*>(p.C);
+  // B and C rows of the group
+  for (int i = threadIdx.x; i < n * N; i += THREADS) {
+    const int tt = i / N, k = i - tt * N;
+    const int64_t r = r0 + t0 + tt;
+    s.B[tt][k] = io_to_float<IT>(Bp[r * p.B_rs + (int64_t)g * p.B_gs + k]);
+    s.C[tt][k] = io_to_float<IT>(Cp[r * p.C_rs + (int64_t)g * p.C_gs + k]);
+  }
+  // per-row scalars
+  const IT* xp = static_cast<const IT*>(p.x);
+  const IT* zp = static_cast<const IT*>(p.z);
+  for (int i = threadIdx.x; i < n * ROWS; i += THREADS) {
+    const int tt = i / ROWS, j = i - tt * ROWS;
+    const int prow = p0 + j;
+    float dA = 1.0f, dtx = 0.0f, Dx = 0.0f, gate = 1.0f;
+    if (prow < p.P) {
+      const int64_t r = r0 + t0 + tt;
+      const float xv = io_to_float<IT>(xp[r * p.x_rs + (int64_t)h * p.x_hs + prow]);
+      float dtv = p.dt[r * p.dt_rs + (int64_t)h * p.dt_hs + (int64_t)prow * p.dt_ds] + bias;
+      if (p.softplus) dtv = softplus_f(dtv);
+      dA = expf(A * dtv);
+      dtx = dtv * xv;
+      Dx = Dh * xv;
+      if (zp) {
+        const float zv = io_to_float<IT>(zp[r * p.z_rs + (int64_t)h * p.z_hs + prow]);
+        gate = zv / (1.0f + expf(-zv));
+      }
+    }
+    s.dA[tt][j] = dA;
+    s.dtx[tt][j] = dtx;
+    s.Dx[tt][j] = Dx;
+    s.gate[tt][j] = gate;
+  }
+}
+
+// One CTA: rows [p0, p0 + ROWS) of head h, sequence rows [r0, r0 + len),
+// state read from `src` (if read_ok), step t written to dst_of(t).
+template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, class DstFn>
+__device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64_t r0, int len,
+                                          int64_t src, bool read_ok, DstFn dst_of) {
+  using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
+  using L = typename Cfg::L;
+  constexpr int ROWS = Cfg::ROWS;
+  constexpr int THREADS = Cfg::THREADS;
+  __shared__ Stage<N, ROWS, LMAX> stg;
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int q = lane % L::LPR;   // chunk lane within the row
+  const int rr = lane / L::LPR;  // row within the warp instruction
+  const int g = h / p.hr;
+  const int64_t block_elems = (int64_t)p.P * N;
+  ST* state = static_cast<ST*>(p.state);
+
+  // 1. issue every state load of this thread's rows
+  uint4 raw[UNR][L::CPL];
+  {
+    const ST* base = state + (((read_ok ? src : 0) * p.H + h) * block_elems);
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int prow = p0 + (warp * UNR + u) * L::RPW + rr;
+      const bool ok = read_ok && prow < p.P;
+#pragma unroll
+      for (int c = 0; c < L::CPL; ++c) {
+        raw[u][c] = ok ? ld_stream(base + (int64_t)prow * N + (q + c * L::LPR) * L::VEC)
+                       : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+
+  // 2. stage the first steps while the loads are in flight
+  const float A = p.A[(int64_t)h * p.A_s];
+  const float Dh = p.D ? p.D[(int64_t)h * p.D_s] : 0.0f;
+  const float bias = p.dt_bias ? p.dt_bias[(int64_t)h * p.bias_s] : 0.0f;
+  int n0 = len < LMAX ? len : LMAX;
+  stage_steps<IT, N, ROWS, LMAX, THREADS>(stg, p, r0, 0, n0, h, g, p0, A, Dh, bias);
+  __syncthreads();
+
+  // 3. widen the state to fp32 registers
+  float hs[UNR][L::EPL];
+#pragma unroll
+  for (int u = 0; u < UNR; ++u)
+#pragma unroll
+    for (int c = 0; c < L::CPL; ++c) Elem<ST>::unpack(raw[u][c], &hs[u][c * L::VEC]);
+
+  IT* out_io = static_cast<IT*>(p.out);
+  float* out_f = static_cast<float*>(p.out);
+
+  for (int t0 = 0; t0 < len; t0 += LMAX) {
+    const int n = (len - t0) < LMAX ? (len - t0) : LMAX;
+    if (t0 > 0) {
+      __syncthreads();  // everyone is done with the previous stage
+      stage_steps<IT, N, ROWS, LMAX, THREADS>(stg, p, r0, t0, n, h, g, p0, A, Dh, bias);
+      __syncthreads();
+    }
+    for (int tt = 0; tt < n; ++tt) {
+      const int64_t r = r0 + t0 + tt;
+      // this lane's B and C values
+      float bv[L::EPL], cv[L::EPL];
+#pragma unroll
+      for (int c = 0; c < L::CPL; ++c) {
+        const int k0 = (q + c * L::LPR) * L::VEC;
+#pragma unroll
+        for (int e = 0; e < L::VEC; e += 4) {
+          const float4 b4 = *reinterpret_cast<const float4*>(&stg.B[tt][k0 + e]);
+          const float4 c4 = *reinterpret_cast<const float4*>(&stg.C[tt][k0 + e]);
+          bv[c * L::VEC + e + 0] = b4.x; bv[c * L::VEC + e + 1] = b4.y;
+          bv[c * L::VEC + e + 2] = b4.z; bv[c * L::VEC + e + 3] = b4.w;
+          cv[c * L::VEC + e + 0] = c4.x; cv[c * L::VEC + e + 1] = c4.y;
+          cv[c * L::VEC + e + 2] = c4.z; cv[c * L::VEC + e + 3] = c4.w;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int j = (warp * UNR + u) * L::RPW + rr;  // row within the CTA tile
+        const float dA = stg.dA[tt][j];
+        const float dtx = stg.dtx[tt][j];
+        float acc0 = 0.0f, acc1 = 0.0f;  // two partial sums: shorter rounding chains
+#pragma unroll
+        for (int e = 0; e < L::EPL; ++e) {
+          const float hv = fmaf(hs[u][e], dA, dtx * bv[e]);
+          hs[u][e] = hv;
+          if (e & 1) acc1 = fmaf(hv, cv[e], acc1);
+          else acc0 = fmaf(hv, cv[e], acc0);
+        }
+        float acc = acc0 + acc1;
+#pragma unroll
+        for (int off = L::LPR / 2; off > 0; off >>= 1)
+          acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const int prow = p0 + j;
+        if (q == 0 && prow < p.P) {
+          const float yv = (acc + stg.Dx[tt][j]) * stg.gate[tt][j];
+          const int64_t o = r * p.o_rs + (int64_t)h * p.o_hs + prow;
+          if (p.out_f32) out_f[o] = yv;
+          else out_io[o] = float_to_io<IT>(yv);
+        }
+      }
+      // write this step's state
+      int64_t dst;
+      if (read_ok && !p.disable && dst_of(t0 + tt, &dst) && slot_ok(dst, p.pad, p.slots)) {
+        ST* base = state + ((dst * p.H + h) * block_elems);
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          const int prow = p0 + (warp * UNR + u) * L::RPW + rr;
+          if (prow < p.P) {
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c)
+              st_state(base + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
+                       Elem<ST>::pack(&hs[u][c * L::VEC]));
+          }
+        }
+      }
+    }
+  }
+}
+
+// One-token decode: blockIdx -> (sequence b, head, row tile).
+template <class ST, class IT, int N, int WARPS, int UNR>
+__global__ void __launch_bounds__(WARPS * 32)
+    ssu_one_token_kernel(const KParams p, const OneTokenArgs a) {
+  int64_t bid = blockIdx.x;
+  const int tile = (int)(bid % p.tiles);
+  bid /= p.tiles;
+  const int h = (int)(bid % p.H);
+  const int64_t b = bid / p.H;
+  using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, 1>;
+  const int p0 = tile * Cfg::ROWS;
+
+  const int64_t src = a.sbi ? load_int(a.sbi, b, a.idx64) : b;
+  const bool read_ok = slot_ok(src, p.pad, p.slots);
+  const int64_t dst = a.dsbi ? load_int(a.dsbi, b, a.idx64) : src;
+  ssu_block<ST, IT, N, WARPS, UNR, 1>(p, h, p0, b, 1, src, read_ok,
+                                      [dst](int, int64_t* o) { *o = dst; return true; });
+}
+
+// Packed varlen / MTP: blockIdx -> (sequence s, head, row tile).
+template <class ST, class IT, int N, int WARPS, int UNR, int LMAX>
+__global__ void __launch_bounds__(WARPS * 32)
+    ssu_varlen_kernel(const KParams p, const VarlenArgs a) {
+  int64_t bid = blockIdx.x;
+  const int tile = (int)(bid % p.tiles);
+  bid /= p.tiles;
+  const int h = (int)(bid % p.H);
+  const int64_t s = bid / p.H;
+  using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
+  const int p0 = tile * Cfg::ROWS;
+
+  int64_t begin, end;
+  if (a.cu) {
+    begin = load_int(a.cu, s, a.meta64);
+    end = load_int(a.cu, s + 1, a.meta64);
+  } else {
+    begin = s * a.dense_steps;
+    end = begin + a.dense_steps;
+  }
+  if (begin < 0) begin = 0;
+  if (end > a.rows) end = a.rows;
+  if (end <= begin) return;  // uniform over the CTA: an empty sequence does nothing
+  const int len = (int)(end - begin);
+
+  int64_t src = s;
+  bool read_ok = true;
+  if (a.src.idx) {
+    const int64_t col = a.na ? load_int(a.na, s, a.meta64) - 1 : 0;
+    read_ok = table_entry(a.src, s, col, a.idx64, &src);
+  }
+  read_ok = read_ok && slot_ok(src, p.pad, p.slots);
+
+  const TableArgs dtab = a.dst.idx ? a.dst : a.src;  // no write table: the read table
+  const int idx64 = a.idx64;
+  auto dst_of = [dtab, idx64, s](int t, int64_t* o) -> bool {
+    if (dtab.idx) return table_entry(dtab, s, t, idx64, o);
+    *o = s;
+    return true;
+  };
+  ssu_block<ST, IT, N, WARPS, UNR, LMAX>(p, h, p0, begin, len, src, read_ok, dst_of);
+}
+
+}  // namespace ssu
