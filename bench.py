@@ -142,10 +142,11 @@ def accounting(case):
 class Step:
     """One pass of the hot path over a resident batch (all device tensors)."""
 
-    def __init__(self, case):
+    def __init__(self, case, algorithm="auto"):
         import mamba2_ssm_decode_gb300 as ssu
         self.ssu = ssu
         self.case = case
+        self.algorithm = algorithm
         self.out = torch.empty_like(case.x)
         self.launches = 1 + (2 if case.ring_start is not None else 0)
         if case.kind == "varlen" and case.cu_seqlens is None:
@@ -165,7 +166,7 @@ class Step:
         out = self.out if out is None else out
         kw = dict(D=c.D, z=z, dt_bias=c.dt_bias, dt_softplus=c.dt_softplus,
                   pad_slot_id=c.pad_slot_id, disable_state_update=c.disable_state_update,
-                  out=out)
+                  out=out, algorithm=self.algorithm)
         if c.kind == "single":
             self.ssu.ssu_update(c.state, x, dt, c.A, B, C, state_batch_indices=sbi,
                                 dst_state_batch_indices=c.dst_state_batch_indices, **kw)
@@ -392,10 +393,10 @@ def cpu_baseline(case, min_seconds=10.0):
                       f"{secs:.1f} s on one host core (fp64 C oracle)"}
 
 
-def measure(name, device, seed, steps, warmup, stream):
+def measure(name, device, seed, steps, warmup, stream, algorithm="auto"):
     case = _workload(name, device, seed)
     tokens, ssu_bytes, trk_bytes = accounting(case)
-    step = Step(case)
+    step = Step(case, algorithm)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             step()
@@ -467,7 +468,7 @@ def run_ours(args):
 
     case = _workload(args.workload, device, seed)
     tokens, ssu_bytes, _ = accounting(case)
-    step = Step(case)
+    step = Step(case, args.algorithm)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
@@ -506,6 +507,7 @@ def run_ours(args):
         "config": {"workload": case.name, "batch": case.nseqs, "nheads": H, "headdim": P,
                    "dstate": N, "ngroups": G, "state_dtype": str(case.state.dtype)[6:],
                    "io_dtype": str(case.x.dtype)[6:], "slots": slots, "non_pad_tokens": tokens,
+                   "algorithm": args.algorithm,
                    "l2": f"no flush: each step touches {ssu_bytes / 1e9:.2f} GB > 129 MB L2",
                    "parallelism": f"replicas x{world} (weak; independent sequence shards)"},
         "hbm_gbs": achieved,
@@ -523,7 +525,8 @@ def run_ours(args):
         del case, step
         torch.cuda.empty_cache()
         for name in EXTRAS:
-            c2, s2, r = measure(name, device, args.seed, max(5, min(args.steps, 50)), 3, stream)
+            c2, s2, r = measure(name, device, args.seed, max(5, min(args.steps, 50)), 3, stream,
+                                args.algorithm)
             r["frac"] = r["gbs"] / peak
             line["workloads"][c2.name] = {k: r[k] for k in ("tokens_per_s", "gbs", "frac",
                                                              "launch_ms", "ms_per_step")}
@@ -637,6 +640,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--algorithm", choices=["auto", "direct", "bulk"], default="auto")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

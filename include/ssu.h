@@ -60,6 +60,25 @@ typedef enum ssu_status {
   SSU_ERR_CUDA = 3              /* the kernel launch failed */
 } ssu_status;
 
+/*
+ * Kernel selection (the pages' SSU entry points carry an `algorithm` choice
+ * too: "ssu_dispatch" forwards MambaConfig.ssu_algorithm, "mate.mamba"
+ * accepts auto/simple/vertical/horizontal and runs one kernel for all).
+ *   SSU_ALGO_AUTO    the library's choice (the bulk-copy pipeline whenever a
+ *                    state tile fits its shared-memory stages)
+ *   SSU_ALGO_DIRECT  one CTA per (sequence, head, 64-row tile); each thread
+ *                    loads its state chunks straight into registers
+ *   SSU_ALGO_BULK    persistent CTAs; a producer warp streams each tile into a
+ *                    ring of shared-memory stages with one bulk asynchronous
+ *                    copy while consumer warps compute
+ * Both compute the same arithmetic in the same order (bit-identical results).
+ */
+typedef enum ssu_algorithm {
+  SSU_ALGO_AUTO = 0,
+  SSU_ALGO_DIRECT = 1,
+  SSU_ALGO_BULK = 2
+} ssu_algorithm;
+
 typedef enum ssu_dtype {
   SSU_F32 = 0,
   SSU_BF16 = 1,
@@ -93,6 +112,7 @@ typedef enum ssu_dtype {
  * dt_softplus, disable_state_update: flags (0 / 1).
  * pad_slot_id: slot id that marks a padded entry (vLLM passes its null
  *            block id; "mate.mamba" defaults to -1).
+ * algorithm  an ssu_algorithm (0 = auto).
  */
 typedef struct ssu_params {
   void* state;
@@ -121,6 +141,7 @@ typedef struct ssu_params {
   int dt_softplus;
   int disable_state_update;
   int64_t pad_slot_id;
+  int algorithm; /* ssu_algorithm */
 } ssu_params;
 
 /*
@@ -238,6 +259,15 @@ ssu_status ssu_ring_commit(int32_t* ring_start, int64_t ring_start_len,
                            ssu_dtype meta_dtype, int64_t nseqs,
                            int32_t logical_window, int32_t ring_buffer_len,
                            int64_t pad_slot_id, struct CUstream_st* stream);
+
+/*
+ * Device-side error word of the current device: nonzero after a kernel gave
+ * up a bounded wait (bit 1: a tile copy never landed; bit 2: a stage was never
+ * released).  No valid call sets it; it exists so that a fault in the copy
+ * engine ends a kernel instead of hanging it.  This call SYNCHRONISES the
+ * current device; reset != 0 clears the word afterwards.
+ */
+ssu_status ssu_device_error(unsigned int* value, int reset);
 
 /* Static description of a status code. */
 const char* ssu_status_string(ssu_status status);

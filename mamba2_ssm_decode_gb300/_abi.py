@@ -18,6 +18,10 @@ SSU_ERR_INVALID_ARGUMENT = 1
 SSU_ERR_UNSUPPORTED = 2
 SSU_ERR_CUDA = 3
 
+# ssu_algorithm
+SSU_ALGO_AUTO, SSU_ALGO_DIRECT, SSU_ALGO_BULK = 0, 1, 2
+ALGORITHMS = {"auto": SSU_ALGO_AUTO, "direct": SSU_ALGO_DIRECT, "bulk": SSU_ALGO_BULK}
+
 # ssu_dtype
 SSU_F32, SSU_BF16, SSU_F16, SSU_I32, SSU_I64 = 0, 1, 2, 3, 4
 
@@ -50,6 +54,7 @@ class SSUParams(ctypes.Structure):
         ("dt_bias", _c_p), ("dt_bias_stride", _c_i64),
         ("dt_softplus", _c_int), ("disable_state_update", _c_int),
         ("pad_slot_id", _c_i64),
+        ("algorithm", _c_int),
     ]
 
 
@@ -92,6 +97,8 @@ def lib() -> ctypes.CDLL:
         L.ssu_status_string.argtypes = [_c_int]
         L.ssu_last_error.restype = ctypes.c_char_p
         L.ssu_last_error.argtypes = []
+        L.ssu_device_error.restype = _c_int
+        L.ssu_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _c_int]
         L.ssu_abi_version.restype = _c_int
         L.ssu_abi_version.argtypes = []
         if L.ssu_abi_version() != ABI_VERSION:

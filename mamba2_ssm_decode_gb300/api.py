@@ -88,7 +88,7 @@ def _per_head(t, heads, name):
 
 
 def _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
-            disable_state_update, rows):
+            disable_state_update, rows, algorithm="auto"):
     if state.dim() != 4:
         raise ValueError(f"state must be [slots, heads, dim, dstate], got {tuple(state.shape)}")
     if not state.is_contiguous():
@@ -141,25 +141,30 @@ def _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
     p.dt_softplus = int(bool(dt_softplus))
     p.disable_state_update = int(bool(disable_state_update))
     p.pad_slot_id = int(pad_slot_id)
+    if algorithm not in _abi.ALGORITHMS:
+        raise ValueError(f"algorithm must be one of {sorted(_abi.ALGORITHMS)}, got {algorithm!r}")
+    p.algorithm = _abi.ALGORITHMS[algorithm]
     return p
 
 
 def ssu_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
                state_batch_indices=None, dst_state_batch_indices=None, pad_slot_id=-1,
-               out=None, disable_state_update=False, out_dtype=None, stream=None):
+               out=None, disable_state_update=False, out_dtype=None, algorithm="auto",
+               stream=None):
     """One-token selective state update (C ABI ``ssu_update``).
 
     state [slots, H, P, N] (updated in place); x, z [batch, H, P]; dt [batch, H]
     or [batch, H, P] fp32; B, C [batch, G, N]; A, D, dt_bias per head fp32;
     slot vectors [batch] int32/int64.  Returns ``out`` [batch, H, P] (x dtype,
-    or ``out_dtype=torch.float32``)."""
+    or ``out_dtype=torch.float32``).  ``algorithm``: "auto", "direct" or "bulk"
+    (the two kernels of the library; identical results)."""
     dev = _require_cuda(state, x, dt, A, B, C, D, z, dt_bias, state_batch_indices,
                         dst_state_batch_indices, out)
     batch = x.shape[0]
     if out is None:
         out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=dev)
     p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
-                disable_state_update, batch)
+                disable_state_update, batch, algorithm)
     idx_dt = 0
     for name, t in (("state_batch_indices", state_batch_indices),
                     ("dst_state_batch_indices", dst_state_batch_indices)):
@@ -196,7 +201,8 @@ def _table(t, name):
 def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
                       cu_seqlens=None, num_accepted_tokens=None, state_batch_indices=None,
                       dst_state_batch_indices=None, pad_slot_id=-1, out=None,
-                      disable_state_update=False, nseqs=None, out_dtype=None, stream=None):
+                      disable_state_update=False, nseqs=None, out_dtype=None, algorithm="auto",
+                      stream=None):
     """Packed varlen / MTP selective state update (C ABI ``ssu_update_varlen``).
 
     x is packed [rows, H, P] with ``cu_seqlens`` [S + 1], or dense
@@ -243,7 +249,7 @@ def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
     if out is None:
         out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=dev)
     p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
-                disable_state_update, rows)
+                disable_state_update, rows, algorithm)
     meta_dt = 0
     if cu_seqlens is not None:
         if cu_seqlens.dim() != 1 or cu_seqlens.numel() != nseqs + 1:
@@ -286,6 +292,13 @@ def _tracker_args(ring_start, prev_num_accepted, prev_query_len, state_batch_ind
     nseqs = sbi.shape[0]
     stride = sbi.stride(0)   # column 0 of a 2-D table
     return nseqs, stride, _int_dtype(sbi, "state_batch_indices")
+
+
+def ssu_device_error(reset=False):
+    """The current device's error word (C ABI ``ssu_device_error``; synchronises)."""
+    v = ctypes.c_uint(0)
+    _abi.check(_abi.lib().ssu_device_error(ctypes.byref(v), int(bool(reset))))
+    return v.value
 
 
 def ssu_ring_update(ring_start, prev_num_accepted, prev_query_len, state_batch_indices,

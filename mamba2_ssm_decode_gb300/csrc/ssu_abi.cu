@@ -7,10 +7,48 @@
 // tracker wrappers on "vllm.model_executor.layers.mamba.ops.ssu_dispatch".
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "../../include/ssu.h"
 #include "ssu_launch.cuh"
+
+namespace ssu {
+constexpr int kMaxDevices = 64;
+}
+
+// Error word of the bulk-copy kernels (one per device: module memory).
+__device__ unsigned int g_ssu_device_error = 0;
+
+namespace ssu {
+
+unsigned* device_error_word() {
+  static std::mutex mu;
+  static unsigned* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_ssu_device_error) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned*>(a);
+  }
+  return addr[dev];
+}
+
+int sm_count() {
+  static int count[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  if (count[dev] == 0) {
+    int c = 0;
+    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+    count[dev] = c > 0 ? c : 1;
+  }
+  return count[dev];
+}
+
+}  // namespace ssu
 
 namespace {
 
@@ -79,6 +117,10 @@ ssu_status check_params(const ssu_params* p, ssu::KParams* k) {
     return fail(SSU_ERR_INVALID_ARGUMENT, "state must be 16-byte aligned");
   if (!p->x || !p->out || !p->dt || !p->B || !p->C || !p->A)
     return fail(SSU_ERR_INVALID_ARGUMENT, "x, out, dt, B, C and A must not be NULL");
+  if (p->algorithm != SSU_ALGO_AUTO && p->algorithm != SSU_ALGO_DIRECT &&
+      p->algorithm != SSU_ALGO_BULK)
+    return fail(SSU_ERR_INVALID_ARGUMENT, "algorithm must be auto, direct or bulk, got %d",
+                p->algorithm);
 
   k->state = p->state;
   k->slots = p->slots;
@@ -124,9 +166,12 @@ cudaError_t dispatch(const ssu_params* p, bool varlen, const ssu::KParams& k,
   const bool io_bf16 = p->io_dtype == SSU_BF16;
   const int N = (int)p->dstate;
   switch (p->state_dtype) {
-    case SSU_F32: return ssu::launch_state_f32(N, io_bf16, varlen, k, oa, va, nitems, stream);
-    case SSU_BF16: return ssu::launch_state_bf16(N, io_bf16, varlen, k, oa, va, nitems, stream);
-    case SSU_F16: return ssu::launch_state_f16(N, io_bf16, varlen, k, oa, va, nitems, stream);
+    case SSU_F32:
+      return ssu::launch_state_f32(N, io_bf16, varlen, k, oa, va, nitems, stream, p->algorithm);
+    case SSU_BF16:
+      return ssu::launch_state_bf16(N, io_bf16, varlen, k, oa, va, nitems, stream, p->algorithm);
+    case SSU_F16:
+      return ssu::launch_state_f16(N, io_bf16, varlen, k, oa, va, nitems, stream, p->algorithm);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -288,6 +333,19 @@ ssu_status ssu_ring_commit(int32_t* ring_start, int64_t ring_start_len,
       index_dtype == SSU_I64, num_accepted_tokens, query_start_loc, meta_dtype == SSU_I64, nseqs,
       num_states, logical_window, ring_buffer_len, pad_slot_id, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+ssu_status ssu_device_error(unsigned int* value, int reset) {
+  if (!value) return fail(SSU_ERR_INVALID_ARGUMENT, "value must not be NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(value, g_ssu_device_error, sizeof(unsigned));
+  if (e == cudaSuccess && reset) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_ssu_device_error, &zero, sizeof zero);
+  }
+  if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "reading the error word failed: %s",
+                                    cudaGetErrorString(e));
   return ok();
 }
 

@@ -1,9 +1,15 @@
 // ssu_launch.cuh -- tile configuration and typed launchers of the SSU kernels.
 #pragma once
 
-#include "ssu_kernel.cuh"
+#include <algorithm>
+
+#include "ssu_bulk.cuh"
 
 namespace ssu {
+
+// Host helpers defined in ssu_abi.cu.
+unsigned* device_error_word();  // this device's error word (device address)
+int sm_count();                 // SMs of the current device
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
@@ -19,11 +25,55 @@ struct Tune {
   static constexpr int LMAX = 4;
 };
 
+// Bulk-copy pipeline per (state dtype, dstate, staged steps): the same
+// 4-warp x 64-row consumer tile as Tune, plus a producer warp, with as many
+// shared-memory stages (2..4) as let two CTAs share an SM.
+template <class ST, int N, int LMAX>
+struct BulkTune {
+  using T = Tune<ST, N>;
+  using L = typename T::L;
+  static constexpr int WARPS = T::WARPS;
+  static constexpr int UNR = T::UNR;
+  static constexpr int ROWS = WARPS * L::RPW * UNR;
+  static constexpr int PER_STAGE = ROWS * N * (int)sizeof(ST) + LMAX * (2 * N + 4 * ROWS) * 4;
+  static constexpr int BUDGET = 110 * 1024;  // two CTAs per SM
+  static constexpr int S = (4 * PER_STAGE <= BUDGET) ? 4 : (3 * PER_STAGE <= BUDGET) ? 3 : 2;
+};
+
+template <class ST, class IT, int N, bool VARLEN>
+cudaError_t launch_bulk(KParams p, const OneTokenArgs& oa, const VarlenArgs& va, int64_t nitems,
+                        cudaStream_t stream) {
+  constexpr int LMAX = VARLEN ? Tune<ST, N>::LMAX : 1;
+  using BT = BulkTune<ST, N, LMAX>;
+  using Cfg = BulkConfig<ST, IT, N, BT::WARPS, BT::UNR, BT::S, LMAX>;
+  auto kern = ssu_bulk_kernel<ST, IT, N, BT::WARPS, BT::UNR, BT::S, LMAX, VARLEN>;
+  p.tiles = (p.P + Cfg::ROWS - 1) / Cfg::ROWS;
+  const int64_t items = nitems * (int64_t)p.H * p.tiles;
+  if (items <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Cfg::THREADS, Cfg::SMEM);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int64_t grid = std::min<int64_t>(items, (int64_t)sm_count() * per_sm);
+  unsigned* err = device_error_word();
+  if (!err) return cudaErrorInvalidSymbol;
+  kern<<<(unsigned)grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p, oa, va, items, err);
+  return cudaGetLastError();
+}
+
 template <class ST, class IT, int N>
 cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const VarlenArgs* va,
-                         int64_t nitems, cudaStream_t stream) {
+                         int64_t nitems, cudaStream_t stream, int algorithm) {
   using T = Tune<ST, N>;
   using Cfg = SSUConfig<ST, IT, N, T::WARPS, T::UNR, T::LMAX>;
+  if (algorithm != 1 /* SSU_ALGO_DIRECT */) {
+    const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
+    const VarlenArgs v0 = va ? *va : VarlenArgs{};
+    return varlen ? launch_bulk<ST, IT, N, true>(p, o0, v0, nitems, stream)
+                  : launch_bulk<ST, IT, N, false>(p, o0, v0, nitems, stream);
+  }
   p.tiles = (p.P + Cfg::ROWS - 1) / Cfg::ROWS;
   const int64_t grid = nitems * (int64_t)p.H * p.tiles;
   if (grid <= 0) return cudaSuccess;
@@ -40,13 +90,13 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
 
 template <class ST, class IT>
 cudaError_t launch_io(int N, bool varlen, const KParams& p, const OneTokenArgs* oa,
-                      const VarlenArgs* va, int64_t nitems, cudaStream_t stream) {
+                      const VarlenArgs* va, int64_t nitems, cudaStream_t stream, int algo) {
   switch (N) {
-    case 16: return launch_typed<ST, IT, 16>(varlen, p, oa, va, nitems, stream);
-    case 32: return launch_typed<ST, IT, 32>(varlen, p, oa, va, nitems, stream);
-    case 64: return launch_typed<ST, IT, 64>(varlen, p, oa, va, nitems, stream);
-    case 128: return launch_typed<ST, IT, 128>(varlen, p, oa, va, nitems, stream);
-    case 256: return launch_typed<ST, IT, 256>(varlen, p, oa, va, nitems, stream);
+    case 16: return launch_typed<ST, IT, 16>(varlen, p, oa, va, nitems, stream, algo);
+    case 32: return launch_typed<ST, IT, 32>(varlen, p, oa, va, nitems, stream, algo);
+    case 64: return launch_typed<ST, IT, 64>(varlen, p, oa, va, nitems, stream, algo);
+    case 128: return launch_typed<ST, IT, 128>(varlen, p, oa, va, nitems, stream, algo);
+    case 256: return launch_typed<ST, IT, 256>(varlen, p, oa, va, nitems, stream, algo);
   }
   return cudaErrorInvalidValue;
 }
@@ -54,13 +104,13 @@ cudaError_t launch_io(int N, bool varlen, const KParams& p, const OneTokenArgs* 
 // defined in ssu_state_{f32,bf16,f16}.cu
 cudaError_t launch_state_f32(int N, bool io_bf16, bool varlen, const KParams& p,
                              const OneTokenArgs* oa, const VarlenArgs* va, int64_t nitems,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int algorithm);
 cudaError_t launch_state_bf16(int N, bool io_bf16, bool varlen, const KParams& p,
                               const OneTokenArgs* oa, const VarlenArgs* va, int64_t nitems,
-                              cudaStream_t stream);
+                              cudaStream_t stream, int algorithm);
 cudaError_t launch_state_f16(int N, bool io_bf16, bool varlen, const KParams& p,
                              const OneTokenArgs* oa, const VarlenArgs* va, int64_t nitems,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int algorithm);
 
 // defined in ring_trackers.cu
 cudaError_t launch_ring_update(int32_t* rs, int32_t* pna, int32_t* pql, const void* sbi,

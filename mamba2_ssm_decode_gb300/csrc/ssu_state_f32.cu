@@ -5,9 +5,9 @@ namespace ssu {
 
 cudaError_t launch_state_f32(int N, bool io_bf16, bool varlen, const KParams& p,
                               const OneTokenArgs* oa, const VarlenArgs* va, int64_t nitems,
-                              cudaStream_t stream) {
-  return io_bf16 ? launch_io<float, __nv_bfloat16>(N, varlen, p, oa, va, nitems, stream)
-                 : launch_io<float, __half>(N, varlen, p, oa, va, nitems, stream);
+                              cudaStream_t stream, int algorithm) {
+  return io_bf16 ? launch_io<float, __nv_bfloat16>(N, varlen, p, oa, va, nitems, stream, algorithm)
+                 : launch_io<float, __half>(N, varlen, p, oa, va, nitems, stream, algorithm);
 }
 
 }  // namespace ssu

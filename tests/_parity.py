@@ -23,11 +23,11 @@ STATE_TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-2, torch.float16: 2e-2}
 HALF_ULP_REL = {torch.bfloat16: 2.0**-8, torch.float16: 2.0**-11, torch.float32: 0.0}
 
 
-def run_gpu(case, out_dtype=None):
+def run_gpu(case, out_dtype=None, algorithm="auto"):
     """Call the CUDA path for a case whose tensors live on the GPU; returns out."""
     kw = dict(D=case.D, z=case.z, dt_bias=case.dt_bias, dt_softplus=case.dt_softplus,
               pad_slot_id=case.pad_slot_id, disable_state_update=case.disable_state_update,
-              out_dtype=out_dtype)
+              out_dtype=out_dtype, algorithm=algorithm)
     if case.kind == "single":
         return ssu.ssu_update(case.state, case.x, case.dt, case.A, case.B, case.C,
                               state_batch_indices=case.state_batch_indices,
@@ -104,16 +104,17 @@ def compare_pool(pool_gpu, pool_ref, pool_before, label=""):
     return ratio, int(changed.sum())
 
 
-def parity(oracle, case_gpu, out_dtype=None, label=""):
+def parity(oracle, case_gpu, out_dtype=None, label="", algorithm="auto"):
     """Full-size parity of every element: GPU call vs oracle on host copies."""
     cpu = case_gpu.to("cpu")
     before = cpu.state.clone()
     y_ref = run_oracle(oracle, cpu)
-    out = run_gpu(case_gpu, out_dtype)
+    out = run_gpu(case_gpu, out_dtype, algorithm)
     torch.cuda.synchronize()
     covered = ~torch.isnan(y_ref.reshape(y_ref.shape[0], -1)).any(dim=1)
     ry = compare_y(out, y_ref, cpu.state.dtype, rows=covered, label=label)
     rs, nchanged = compare_pool(case_gpu.state, cpu.state, before, label=label)
+    assert ssu.ssu_device_error() == 0, f"{label}: device error word set"
     return {"y_err": ry, "state_err": rs, "slots_written": nchanged}
 
 
@@ -183,12 +184,12 @@ def subset(case_gpu, seqs):
     return sub, rows, remap
 
 
-def sampled_parity(oracle, case_gpu, seqs, out_dtype=None, label=""):
+def sampled_parity(oracle, case_gpu, seqs, out_dtype=None, label="", algorithm="auto"):
     """Parity of the sequences `seqs` of a full-size call made on the GPU: the
     oracle runs on their rows and slots only (copied before the call)."""
     sub, rows, remap = subset(case_gpu, seqs)
     before = sub.state.clone()
-    out = run_gpu(case_gpu, out_dtype)
+    out = run_gpu(case_gpu, out_dtype, algorithm)
     torch.cuda.synchronize()
     y_ref = run_oracle(oracle, sub)
     ry = compare_y(out[torch.tensor(rows, device=out.device)], y_ref, sub.state.dtype,

@@ -29,26 +29,29 @@ def _built():
 
 SDT = [torch.float32, torch.bfloat16, torch.float16]
 IODT = [torch.bfloat16, torch.float16]
+ALGOS = ["direct", "bulk"]
 
 
 # ---------------------------------------------------------------------------
 # one-token route
 # ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("sdt", SDT)
 @pytest.mark.parametrize("iodt", IODT)
 @pytest.mark.parametrize("N", [16, 32, 64, 128, 256])
-def test_one_token_dtypes_and_dstate(oracle_mod, sdt, iodt, N):
+def test_one_token_dtypes_and_dstate(oracle_mod, sdt, iodt, N, algo):
     case = W.single_token_case(batch=7, heads=6, headdim=80, dstate=N, groups=3, slots=20,
                                state_dtype=sdt, io_dtype=iodt, pad_frac=0.3, seed=N,
                                device=DEV)
-    P.parity(oracle_mod, case, label=f"{sdt} {iodt} N={N}")
+    P.parity(oracle_mod, case, label=f"{sdt} {iodt} N={N} {algo}", algorithm=algo)
 
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("variant", ["no_z", "no_D_bias", "dt_per_dim", "dt_h1", "no_softplus",
                                      "dst_table", "in_range_pad", "out_f32", "int64",
                                      "identity", "disable", "P_ragged", "tied_A"])
-def test_one_token_variants(oracle_mod, variant):
+def test_one_token_variants(oracle_mod, variant, algo):
     kw = dict(batch=9, heads=4, headdim=64, dstate=128, groups=2, slots=24,
               state_dtype=torch.float32, pad_frac=0.2, seed=7, device=DEV)
     if variant == "no_z":
@@ -84,7 +87,7 @@ def test_one_token_variants(oracle_mod, variant):
         case.state_batch_indices = None
     if variant == "tied_A":
         case.A = case.A[:, None, None].expand(4, 64, 128)
-    P.parity(oracle_mod, case, out_dtype=out_dtype, label=variant)
+    P.parity(oracle_mod, case, out_dtype=out_dtype, label=variant, algorithm=algo)
 
 
 def test_one_token_strided_operands_bit_exact():
@@ -114,19 +117,21 @@ def test_one_token_strided_operands_bit_exact():
 # packed varlen / MTP route
 # ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("sdt", SDT)
-@pytest.mark.parametrize("N", [16, 64, 128])
-def test_varlen_dtypes(oracle_mod, sdt, N):
+@pytest.mark.parametrize("N", [16, 64, 128, 256])
+def test_varlen_dtypes(oracle_mod, sdt, N, algo):
     case = W.varlen_case(nseqs=9, max_len=6, heads=4, headdim=80, dstate=N, groups=2, slots=160,
                          state_dtype=sdt, pad_frac=0.25, seed=11 + N, device=DEV)
-    P.parity(oracle_mod, case, label=f"varlen {sdt} N={N}")
+    P.parity(oracle_mod, case, label=f"varlen {sdt} N={N} {algo}", algorithm=algo)
 
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("variant", ["empty_seqs", "no_counts", "flat_tables", "dense",
                                      "same_table", "int64", "disable", "no_dst_no_src",
                                      "count_out_of_table", "long_chain", "out_f32",
                                      "dt_per_dim", "f16_io"])
-def test_varlen_variants(oracle_mod, variant):
+def test_varlen_variants(oracle_mod, variant, algo):
     kw = dict(nseqs=7, max_len=4, heads=4, headdim=64, dstate=128, groups=2, slots=80,
               state_dtype=torch.float32, pad_frac=0.15, seed=23, device=DEV)
     if variant == "dense":
@@ -172,7 +177,20 @@ def test_varlen_variants(oracle_mod, variant):
         case.num_accepted_tokens = na
     if variant == "out_f32":
         out_dtype = torch.float32
-    P.parity(oracle_mod, case, out_dtype=out_dtype, label=variant)
+    P.parity(oracle_mod, case, out_dtype=out_dtype, label=variant, algorithm=algo)
+
+
+@pytest.mark.parametrize("make", ["mamba2_2p7b_decode", "hybrid_grouped_decode", "mtp_varlen"])
+def test_algorithms_bit_identical(make):
+    """The register kernel and the bulk-copy pipeline give the same bits."""
+    a = getattr(W, make)(device=DEV)
+    b = a.clone()
+    ya = P.run_gpu(a, algorithm="direct")
+    yb = P.run_gpu(b, algorithm="bulk")
+    assert torch.equal(ya, yb)
+    assert torch.equal(a.state, b.state)
+    import mamba2_ssm_decode_gb300 as ssu
+    assert ssu.ssu_device_error() == 0
 
 
 def test_varlen_with_length_one_equals_one_token_bit_exact():
