@@ -59,7 +59,8 @@ def _load():
             lib.oracle_ssu_update.restype = _int
             lib.oracle_ssu_update.argtypes = (
                 [_p, _int, _i64, _i64, _i64, _i64, _i64, _i64,
-                 _p, _p, _int, _p, _int, _p, _p, _p, _p, _p, _p, _p, _i64, _int, _int, _p])
+                 _p, _p, _int, _p, _int, _p, _p, _p, _p, _p, _p, _p, _i64, _int, _int, _int,
+                 _p])
             lib.oracle_ssu_update_varlen.restype = _int
             lib.oracle_ssu_update_varlen.argtypes = (
                 [_p, _int, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
@@ -67,7 +68,7 @@ def _load():
                  _p, _i64, _p,
                  _p, _i64, _i64, _i64, _i64,
                  _p, _i64, _i64, _i64, _i64,
-                 _i64, _int, _int, _p])
+                 _i64, _int, _int, _int, _p])
             lib.oracle_ring_update.restype = _int
             lib.oracle_ring_update.argtypes = (
                 [_p, _i64, _p, _i64, _p, _i64, _p, _i64, _i64, _int, _i32, _i32, _i64])
@@ -99,6 +100,28 @@ def _cpu(t, dtype=None):
     return t.contiguous()
 
 
+def _params(A, D, dt_bias, H, P):
+    """fp32 CPU copies of A, D, dt_bias and the per-(head, dim) bit mask: each is
+    [H] (per head) or [H, P] (per channel; a [H, P, N] view with zero dstate
+    stride or [H, 1] collapse to these)."""
+    mask = 0
+    out = []
+    for bit, t in ((1, A), (2, D), (4, dt_bias)):
+        if t is None:
+            out.append(None)
+            continue
+        t = t.detach().to("cpu", torch.float32)
+        if t.dim() == 3:
+            t = t[:, :, 0]
+        if t.dim() == 2 and t.shape[1] == 1:
+            t = t[:, 0]
+        if t.dim() == 2:
+            assert tuple(t.shape) == (H, P)
+            mask |= bit
+        out.append(t.contiguous())
+    return out[0], out[1], out[2], mask
+
+
 def _check_io(x, z, B, C):
     io = x.dtype
     assert io in (torch.bfloat16, torch.float16), io
@@ -114,7 +137,7 @@ def ssu_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=
 
     state: [slots, H, P, N] CPU tensor, updated IN PLACE (must be contiguous).
     x, z: [batch, H, P]; dt: [batch, H] (per head) or [batch, H, P];
-    B, C: [batch, G, N]; A, D, dt_bias: [H] fp32.  Returns y as float64
+    B, C: [batch, G, N]; A, D, dt_bias: [H] or [H, P] fp32.  Returns y as float64
     [batch, H, P] (unrounded).
     """
     lib = _load()
@@ -126,7 +149,7 @@ def ssu_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=
     x, z, B, C = _cpu(x), _cpu(z), _cpu(B), _cpu(C)
     dt = _cpu(dt, torch.float32)
     dt_per_dim = int(dt.dim() == 3 and dt.shape[2] != 1)
-    A, D, dt_bias = _cpu(A, torch.float32), _cpu(D, torch.float32), _cpu(dt_bias, torch.float32)
+    A, D, dt_bias, per_dim = _params(A, D, dt_bias, H, P)
     sbi = _cpu(state_batch_indices, torch.int64)
     dsbi = _cpu(dst_state_batch_indices, torch.int64)
     y = torch.empty((batch, H, P), dtype=torch.float64)
@@ -134,7 +157,7 @@ def ssu_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=
         _ptr(state), _DT[state.dtype], slots, H, P, N, G, batch,
         _ptr(x), _ptr(z), io, _ptr(dt), dt_per_dim, _ptr(A), _ptr(D), _ptr(dt_bias),
         _ptr(B), _ptr(C), _ptr(sbi), _ptr(dsbi), int(pad_slot_id), int(bool(dt_softplus)),
-        int(bool(disable_state_update)), _ptr(y))
+        int(bool(disable_state_update)), per_dim, _ptr(y))
     if rc != 0:
         raise ValueError(f"oracle_ssu_update rejected its arguments (code {rc})")
     return y
@@ -174,7 +197,7 @@ def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
     x, z, B, C = _cpu(x), _cpu(z), _cpu(B), _cpu(C)
     dt = _cpu(dt, torch.float32)
     dt_per_dim = int(dt.dim() == 3 and dt.shape[2] != 1)
-    A, D, dt_bias = _cpu(A, torch.float32), _cpu(D, torch.float32), _cpu(dt_bias, torch.float32)
+    A, D, dt_bias, per_dim = _params(A, D, dt_bias, H, P)
     cu = _cpu(cu_seqlens, torch.int64)
     if nseqs is None:
         if cu is not None:
@@ -193,7 +216,8 @@ def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
         _ptr(B), _ptr(C), _ptr(cu), int(dense_steps), _ptr(na),
         _ptr(src[0]), src[1], src[2], src[3], src[4],
         _ptr(dst[0]), dst[1], dst[2], dst[3], dst[4],
-        int(pad_slot_id), int(bool(dt_softplus)), int(bool(disable_state_update)), _ptr(y))
+        int(pad_slot_id), int(bool(dt_softplus)), int(bool(disable_state_update)), per_dim,
+        _ptr(y))
     if rc != 0:
         raise ValueError(f"oracle_ssu_update_varlen rejected its arguments (code {rc})")
     return y

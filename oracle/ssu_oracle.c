@@ -28,6 +28,10 @@
  *         y[p] = sum_n h[p][n] * C[g][n] + D[h] * x[p];  y *= silu(z[p])
  *     with g = h / (heads / groups).
  *
+ * A, D and dt_bias are per head ([H], "mate.mamba" _per_head's tied form) or,
+ * flagged per parameter, per (head, dim) channel ([H, P], _per_head's
+ * channel-wise form).
+ *
  * Everything is evaluated in IEEE double from the exact stored input values
  * (bf16 / fp16 / fp32 inputs widen exactly).  Stored state is rounded once,
  * round-to-nearest-even, from the double value to the state dtype.  A chained
@@ -173,6 +177,7 @@ typedef struct {
   const float* A; const float* D; const float* dt_bias;  /* [H]; D, dt_bias may be NULL */
   const void* B; const void* C;                 /* [rows, G, N], io dtype */
   int dt_softplus;
+  int param_per_dim;  /* bit 0: A, bit 1: D, bit 2: dt_bias given per (head, dim) as [H, P] */
 } operands;
 
 /*
@@ -182,10 +187,12 @@ typedef struct {
 static void ssu_step(const operands* o, int64_t r, int64_t h, double* hb, double* y) {
   const int64_t H = o->H, P = o->P, N = o->N;
   const int64_t g = h / (H / o->G); /* heads of one group are contiguous */
-  const double A = o->A[h];
-  const double D = o->D ? o->D[h] : 0.0;
-  const double bias = o->dt_bias ? o->dt_bias[h] : 0.0;
   for (int64_t p = 0; p < P; ++p) {
+    /* per head, or per (head, dim) channel ("mate.mamba", _per_head) */
+    const double A = (o->param_per_dim & 1) ? o->A[h * P + p] : o->A[h];
+    const double D = !o->D ? 0.0 : (o->param_per_dim & 2) ? o->D[h * P + p] : o->D[h];
+    const double bias = !o->dt_bias ? 0.0
+                        : (o->param_per_dim & 4) ? o->dt_bias[h * P + p] : o->dt_bias[h];
     double dt = o->dt_per_dim ? o->dt[(r * H + h) * P + p] : o->dt[r * H + h];
     dt += bias;
     if (o->dt_softplus) dt = softplus(dt);
@@ -225,9 +232,10 @@ int oracle_ssu_update(void* state, int state_dtype, int64_t slots,
                       const float* A, const float* D, const float* dt_bias,
                       const void* B, const void* C,
                       const int64_t* sbi, const int64_t* dsbi, int64_t pad_slot_id,
-                      int dt_softplus, int disable_state_update, double* y) {
+                      int dt_softplus, int disable_state_update, int param_per_dim, double* y) {
   if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0) return 1;
-  operands o = {H, P, N, G, x, z, io_dtype, dt, dt_per_dim, A, D, dt_bias, B, C, dt_softplus};
+  operands o = {H, P, N, G, x, z, io_dtype, dt, dt_per_dim, A, D, dt_bias, B, C, dt_softplus,
+                param_per_dim};
   const int64_t block = P * N;
   double* hb = (double*)malloc(sizeof(double) * (size_t)block);
   if (!hb) return 2;
@@ -292,9 +300,10 @@ int oracle_ssu_update_varlen(void* state, int state_dtype, int64_t slots,
                              const int64_t* dst_tab, int64_t dst_numel, int64_t dst_ss,
                              int64_t dst_ts, int64_t dst_steps,
                              int64_t pad_slot_id, int dt_softplus, int disable_state_update,
-                             double* y) {
+                             int param_per_dim, double* y) {
   if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0) return 1;
-  operands o = {H, P, N, G, x, z, io_dtype, dt, dt_per_dim, A, D, dt_bias, B, C, dt_softplus};
+  operands o = {H, P, N, G, x, z, io_dtype, dt, dt_per_dim, A, D, dt_bias, B, C, dt_softplus,
+                param_per_dim};
   const int64_t block = P * N;
   double* hb = (double*)malloc(sizeof(double) * (size_t)block);
   if (!hb) return 2;

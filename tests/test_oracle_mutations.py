@@ -33,6 +33,8 @@ MUTANTS = {
     "commit_branches_swapped": ("(must_checkpoint ? a : add_i32(acc, a))", "(must_checkpoint ? add_i32(acc, a) : a)"),
     "commit_ignores_pql": ("const int must_checkpoint = pql > 0 && add_i32(acc, pql)",
                            "const int must_checkpoint = add_i32(acc, pql)"),
+    "channel_index_transposed": ("(o->param_per_dim & 1) ? o->A[h * P + p]",
+                                 "(o->param_per_dim & 1) ? o->A[p * H + h]"),
     "bf16_truncates": ("double r = nearbyint(fabs(v) / quantum) * quantum;",
                        "double r = floor(fabs(v) / quantum) * quantum;"),
 }

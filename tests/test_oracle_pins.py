@@ -510,3 +510,53 @@ def test_low_precision_state_is_rounded_once(oracle_mod, sdt):
         # the oracle's double -> bf16 rounding is pinned by the brute-force test above
         want = oracle_mod.round_to(torch.from_numpy(h_new), torch.bfloat16)
     assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+# --------------------------------------------------------------------------
+# per-(head, dim) A / D / dt_bias ("mate.mamba", _per_head's channel-wise form)
+# --------------------------------------------------------------------------
+
+def test_per_channel_params_equal_per_head_when_constant(oracle_mod):
+    a = small_single(torch.float32, seed=81)
+    b = a.clone()
+    P_ = a.x.shape[2]
+    b.A = a.A[:, None].expand(-1, P_).contiguous()
+    b.D = a.D[:, None].expand(-1, P_).contiguous()
+    b.dt_bias = a.dt_bias[:, None, None].expand(-1, P_, 8)   # [H, P, N] view, zero dstate stride
+    ya, yb = run_single(oracle_mod, a), run_single(oracle_mod, b)
+    assert torch.equal(ya, yb) and torch.equal(a.state, b.state)
+
+
+def test_per_channel_decay_is_exact_power_of_two(oracle_mod):
+    """dt = -dt_bias[h, p] with softplus: dt' = ln 2 for every channel, so with
+    B = 0 row p of head h scales by exactly 2^A[h, p]."""
+    case = small_single(torch.float32, seed=82)
+    H, P_ = case.x.shape[1], case.x.shape[2]
+    exps = -(1 + (torch.arange(H * P_) % 3)).reshape(H, P_).to(torch.float32)   # -1, -2, -3
+    case.A = exps
+    case.dt_bias = torch.linspace(-4, -1, H * P_).reshape(H, P_)
+    case.dt = -case.dt_bias[None].expand(case.x.shape[0], -1, -1).contiguous()
+    case.B.zero_()
+    before = case.state.clone()
+    run_single(oracle_mod, case)
+    idx = case.state_batch_indices.long()
+    want = before[idx] * torch.pow(2.0, exps)[None, :, :, None]
+    assert torch.equal(case.state[idx], want)
+
+
+def test_per_channel_zero_state_closed_form(oracle_mod):
+    case = small_single(torch.float32, seed=83)
+    H, P_ = case.x.shape[1], case.x.shape[2]
+    g = torch.Generator().manual_seed(7)
+    case.D = torch.rand(H, P_, generator=g)
+    case.dt_bias = -1 - 3 * torch.rand(H, P_, generator=g)
+    case.state.zero_()
+    y = run_single(oracle_mod, case).numpy()
+    slots, H, P_, N, G = case.dims
+    dtp = softplus_np(f64(case.dt)[:, :, None] + f64(case.dt_bias)[None])      # [b, H, P]
+    Bg = f64(case.B)[:, group_of(H, G), :]
+    Cg = f64(case.C)[:, group_of(H, G), :]
+    bc = np.einsum("bhn,bhn->bh", Bg, Cg)
+    x = f64(case.x)
+    want = x * (dtp * bc[:, :, None] + f64(case.D)[None]) * f64(case.z) * expit(f64(case.z))
+    np.testing.assert_allclose(y, want, rtol=1e-12, atol=1e-12)
