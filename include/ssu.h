@@ -107,8 +107,10 @@ typedef enum ssu_dtype {
  *            dt_dim_stride = 0 is the per-head form [rows, nheads(, 1)].
  * B, C       [rows, ngroups, dstate], io_dtype: element (r, g, n) at
  *            B[r * B_row_stride + g * B_group_stride + n].
- * A, D, dt_bias  fp32 per head: A[h * A_stride]; D and dt_bias may be NULL
- *            (treated as 0).  A stride of 0 ties every head to one value.
+ * A, D, dt_bias  fp32, element (h, p) at A[h * A_stride + p * A_dim_stride]
+ *            (likewise D, dt_bias): a dim stride of 0 is the per-head (tied)
+ *            form, a nonzero one the per-(head, dim) channel form
+ *            ("mate.mamba", _per_head).  D and dt_bias may be NULL (0).
  * dt_softplus, disable_state_update: flags (0 / 1).
  * pad_slot_id: slot id that marks a padded entry (vLLM passes its null
  *            block id; "mate.mamba" defaults to -1).
@@ -133,11 +135,11 @@ typedef struct ssu_params {
   const void* C;
   int64_t C_row_stride, C_group_stride;
   const float* A;
-  int64_t A_stride;
+  int64_t A_stride, A_dim_stride;
   const float* D;
-  int64_t D_stride;
+  int64_t D_stride, D_dim_stride;
   const float* dt_bias;
-  int64_t dt_bias_stride;
+  int64_t dt_bias_stride, dt_bias_dim_stride;
   int dt_softplus;
   int disable_state_update;
   int64_t pad_slot_id;

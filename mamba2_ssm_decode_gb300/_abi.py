@@ -49,9 +49,9 @@ class SSUParams(ctypes.Structure):
         ("dt_dim_stride", _c_i64),
         ("B", _c_p), ("B_row_stride", _c_i64), ("B_group_stride", _c_i64),
         ("C", _c_p), ("C_row_stride", _c_i64), ("C_group_stride", _c_i64),
-        ("A", _c_p), ("A_stride", _c_i64),
-        ("D", _c_p), ("D_stride", _c_i64),
-        ("dt_bias", _c_p), ("dt_bias_stride", _c_i64),
+        ("A", _c_p), ("A_stride", _c_i64), ("A_dim_stride", _c_i64),
+        ("D", _c_p), ("D_stride", _c_i64), ("D_dim_stride", _c_i64),
+        ("dt_bias", _c_p), ("dt_bias_stride", _c_i64), ("dt_bias_dim_stride", _c_i64),
         ("dt_softplus", _c_int), ("disable_state_update", _c_int),
         ("pad_slot_id", _c_i64),
         ("algorithm", _c_int),

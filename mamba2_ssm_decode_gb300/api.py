@@ -67,23 +67,29 @@ def _rows3(t, name, rows, heads, dim):
     return t.stride(0), t.stride(1)
 
 
-def _per_head(t, heads, name):
-    """Stride of a per-head fp32 parameter: [H], [H, 1], or a tied [H, dim, dstate]
-    view with zero inner strides ("mate.mamba", _per_head)."""
+def _per_head(t, heads, dim, name):
+    """(head stride, dim stride) of an fp32 A / D / dt_bias ("mate.mamba",
+    _per_head): per head [H], [H, 1] or a tied [H, dim, dstate] view with zero
+    inner strides (dim stride 0); per (head, dim) channel [H, dim] or a
+    [H, dim, dstate] view with zero dstate stride."""
     if t is None:
-        return 0
+        return 0, 0
     if t.dtype != torch.float32:
         raise NotImplementedError(f"{name} must be fp32, got {t.dtype}")
     if t.shape[0] != heads:
         raise ValueError(f"{name} must have one entry per head ({heads}), got {tuple(t.shape)}")
     if t.dim() == 1:
-        return t.stride(0)
+        return t.stride(0), 0
     if t.dim() == 2 and t.shape[1] == 1:
-        return t.stride(0)
+        return t.stride(0), 0
+    if t.dim() == 2 and t.shape[1] == dim:
+        return t.stride(0), t.stride(1)
     if t.dim() == 3 and t.stride(1) == 0 and t.stride(2) == 0:
-        return t.stride(0)
+        return t.stride(0), 0
+    if t.dim() == 3 and t.shape[1] == dim and t.stride(2) == 0:
+        return t.stride(0), t.stride(1)
     raise NotImplementedError(
-        f"{name}: only per-head (tied) values are implemented; got shape {tuple(t.shape)} "
+        f"{name}: per-head or per-(head, dim) values only; got shape {tuple(t.shape)} "
         f"with strides {t.stride()}")
 
 
@@ -134,10 +140,12 @@ def _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
     p.dt_row_stride, p.dt_head_stride, p.dt_dim_stride = dts
     p.B, p.B_row_stride, p.B_group_stride = B.data_ptr(), B.stride(0), B.stride(1)
     p.C, p.C_row_stride, p.C_group_stride = C.data_ptr(), C.stride(0), C.stride(1)
-    p.A, p.A_stride = A.data_ptr(), _per_head(A, H, "A")
-    p.D, p.D_stride = (D.data_ptr() if D is not None else None), _per_head(D, H, "D")
+    p.A = A.data_ptr()
+    p.A_stride, p.A_dim_stride = _per_head(A, H, P, "A")
+    p.D = D.data_ptr() if D is not None else None
+    p.D_stride, p.D_dim_stride = _per_head(D, H, P, "D")
     p.dt_bias = dt_bias.data_ptr() if dt_bias is not None else None
-    p.dt_bias_stride = _per_head(dt_bias, H, "dt_bias")
+    p.dt_bias_stride, p.dt_bias_dim_stride = _per_head(dt_bias, H, P, "dt_bias")
     p.dt_softplus = int(bool(dt_softplus))
     p.disable_state_update = int(bool(disable_state_update))
     p.pad_slot_id = int(pad_slot_id)

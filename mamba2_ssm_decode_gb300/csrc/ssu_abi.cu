@@ -150,10 +150,13 @@ ssu_status check_params(const ssu_params* p, ssu::KParams* k) {
   k->C_gs = p->C_group_stride;
   k->A = p->A;
   k->A_s = p->A_stride;
+  k->A_ds = p->A_dim_stride;
   k->D = p->D;
   k->D_s = p->D_stride;
+  k->D_ds = p->D_dim_stride;
   k->dt_bias = p->dt_bias;
   k->bias_s = p->dt_bias_stride;
+  k->bias_ds = p->dt_bias_dim_stride;
   k->softplus = p->dt_softplus != 0;
   k->disable = p->disable_state_update != 0;
   k->pad = p->pad_slot_id;

@@ -163,9 +163,6 @@ template <class IT, int N, int ROWS, int LMAX>
 __device__ __forceinline__ void stage_vectors(Stage<N, ROWS, LMAX>& s, const KParams& p,
                                               const Item& it, int t0, int n, int tid, int nthr) {
   const int g = it.h / p.hr;
-  const float A = p.A[(int64_t)it.h * p.A_s];
-  const float Dh = p.D ? p.D[(int64_t)it.h * p.D_s] : 0.0f;
-  const float bias = p.dt_bias ? p.dt_bias[(int64_t)it.h * p.bias_s] : 0.0f;
   const IT* Bp = static_cast<const IT*>(p.B);
   const IT* Cp = static_cast<const IT*>(p.C);
   for (int i = tid; i < n * N; i += nthr) {
@@ -182,6 +179,10 @@ __device__ __forceinline__ void stage_vectors(Stage<N, ROWS, LMAX>& s, const KPa
     float dA = 1.0f, dtx = 0.0f, Dx = 0.0f, gate = 1.0f;
     if (prow < p.P) {
       const int64_t r = it.r0 + t0 + tt;
+      const float A = p.A[(int64_t)it.h * p.A_s + (int64_t)prow * p.A_ds];
+      const float Dh = p.D ? p.D[(int64_t)it.h * p.D_s + (int64_t)prow * p.D_ds] : 0.0f;
+      const float bias =
+          p.dt_bias ? p.dt_bias[(int64_t)it.h * p.bias_s + (int64_t)prow * p.bias_ds] : 0.0f;
       const float xv = io_to_float<IT>(xp[r * p.x_rs + (int64_t)it.h * p.x_hs + prow]);
       float dtv = p.dt[r * p.dt_rs + (int64_t)it.h * p.dt_hs + (int64_t)prow * p.dt_ds] + bias;
       if (p.softplus) dtv = softplus_f(dtv);

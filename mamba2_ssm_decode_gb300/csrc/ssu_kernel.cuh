@@ -55,11 +55,11 @@ struct KParams {
   const void* C;
   int64_t C_rs, C_gs;
   const float* A;
-  int64_t A_s;
+  int64_t A_s, A_ds;  // head and dim strides (dim stride 0: per head)
   const float* D;
-  int64_t D_s;
+  int64_t D_s, D_ds;
   const float* dt_bias;
-  int64_t bias_s;
+  int64_t bias_s, bias_ds;
   int softplus;
   int disable;
   int64_t pad;
@@ -249,8 +249,7 @@ struct __align__(16) Stage {
 // Stage steps [t0, t0 + n) of rows [r0 + t0, ...) for head h / group g.
 template <class IT, int N, int ROWS, int LMAX, int THREADS>
 __device__ __forceinline__ void stage_steps(Stage<N, ROWS, LMAX>& s, const KParams& p,
-                                            int64_t r0, int t0, int n, int h, int g, int p0,
-                                            float A, float Dh, float bias) {
+                                            int64_t r0, int t0, int n, int h, int g, int p0) {
   const IT* Bp = static_cast<const IT*>(p.B);
   const IT* Cp = static_cast<const IT*>(p.C);
   // B and C rows of the group
@@ -269,6 +268,10 @@ __device__ __forceinline__ void stage_steps(Stage<N, ROWS, LMAX>& s, const KPara
     float dA = 1.0f, dtx = 0.0f, Dx = 0.0f, gate = 1.0f;
     if (prow < p.P) {
       const int64_t r = r0 + t0 + tt;
+      const float A = p.A[(int64_t)h * p.A_s + (int64_t)prow * p.A_ds];
+      const float Dh = p.D ? p.D[(int64_t)h * p.D_s + (int64_t)prow * p.D_ds] : 0.0f;
+      const float bias =
+          p.dt_bias ? p.dt_bias[(int64_t)h * p.bias_s + (int64_t)prow * p.bias_ds] : 0.0f;
       const float xv = io_to_float<IT>(xp[r * p.x_rs + (int64_t)h * p.x_hs + prow]);
       float dtv = p.dt[r * p.dt_rs + (int64_t)h * p.dt_hs + (int64_t)prow * p.dt_ds] + bias;
       if (p.softplus) dtv = softplus_f(dtv);
@@ -323,11 +326,8 @@ __device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64
   }
 
   // 2. stage the first steps while the loads are in flight
-  const float A = p.A[(int64_t)h * p.A_s];
-  const float Dh = p.D ? p.D[(int64_t)h * p.D_s] : 0.0f;
-  const float bias = p.dt_bias ? p.dt_bias[(int64_t)h * p.bias_s] : 0.0f;
   int n0 = len < LMAX ? len : LMAX;
-  stage_steps<IT, N, ROWS, LMAX, THREADS>(stg, p, r0, 0, n0, h, g, p0, A, Dh, bias);
+  stage_steps<IT, N, ROWS, LMAX, THREADS>(stg, p, r0, 0, n0, h, g, p0);
   __syncthreads();
 
   // 3. widen the state to fp32 registers
@@ -344,7 +344,7 @@ __device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64
     const int n = (len - t0) < LMAX ? (len - t0) : LMAX;
     if (t0 > 0) {
       __syncthreads();  // everyone is done with the previous stage
-      stage_steps<IT, N, ROWS, LMAX, THREADS>(stg, p, r0, t0, n, h, g, p0, A, Dh, bias);
+      stage_steps<IT, N, ROWS, LMAX, THREADS>(stg, p, r0, t0, n, h, g, p0);
       __syncthreads();
     }
     for (int tt = 0; tt < n; ++tt) {
