@@ -151,7 +151,15 @@ class Step:
         self.launches = 1 + (2 if case.ring_start is not None else 0)
         if case.kind == "varlen" and case.cu_seqlens is None:
             S, T = case.nseqs, case.dense_steps
-            self.v4 = lambda t: None if t is None else t.view(S, T, *t.shape[1:])  # noqa: E731
+
+            def v4(t):   # the dense [batch, steps, ...] view; a per-head dt gets a unit dim
+                if t is None:
+                    return None
+                if t.dim() == 2:
+                    return t.view(S, T, t.shape[1], 1)
+                return t.view(S, T, *t.shape[1:])
+
+            self.v4 = v4
         else:
             self.v4 = None
 

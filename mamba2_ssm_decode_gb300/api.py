@@ -221,7 +221,9 @@ def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
                         state_batch_indices, dst_state_batch_indices, out)
     dense_steps = 1
     dense_out = None
+    dense_shape = None
     if x.dim() == 4:
+        dense_shape = tuple(x.shape)
         batch, steps = x.shape[:2]
         rows = batch * steps
 
@@ -284,7 +286,11 @@ def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
         ctypes.byref(p), nseqs, rows, _ptr(cu_seqlens), dense_steps, _ptr(num_accepted_tokens),
         meta_dt or _abi.SSU_I32, ctypes.byref(src), ctypes.byref(dst), sd or dd or _abi.SSU_I32,
         _stream(dev, stream)))
-    return dense_out if dense_out is not None else out
+    if dense_out is not None:
+        return dense_out
+    if dense_shape is not None:    # a dense call gets its rank back ("mate.mamba")
+        return out.view(dense_shape[:2] + tuple(out.shape[1:]))
+    return out
 
 
 def _tracker_args(ring_start, prev_num_accepted, prev_query_len, state_batch_indices):

@@ -10,14 +10,16 @@
 //
 // Work item = (sequence, head, row tile of ROWS headdim rows); a CTA walks the
 // items blockIdx.x, blockIdx.x + gridDim.x, ...  For item k on stage s = k % S:
-//   producer warp: wait empty[s] (the consumers released item k - S), resolve
-//     the item's slots, arm full[s] with the block's byte count and issue one
-//     bulk copy of the contiguous rows (or just arrive for a pad / invalid read
-//     slot), then stage the item's per-step vectors into stage s and arrive on
-//     full[s] a second time;
-//   consumer warps: wait full[s], read their chunks of the block into fp32
-//     registers, run the steps exactly as the register kernel does (same lane
-//     layout, same arithmetic, same store path), then release empty[s].
+//   producer (one thread): resolve the item's slots (one item ahead, so the
+//     index loads are in flight while it waits), wait empty[s] (the consumers
+//     released item k - S), publish the slots in the stage's record, arm
+//     full[s] with the tile's byte count and issue one bulk copy of its
+//     contiguous rows (or just arrive for a pad / invalid read slot);
+//   consumer warps: stage the item's per-step vectors (B, C, dA, dt' x, D x,
+//     silu z) into one of two shared buffers with one round of loads while the
+//     copy lands, wait full[s], read their chunks of the tile into fp32
+//     registers, release empty[s] at once, then run the steps exactly as the
+//     register kernel does (same lane layout, same arithmetic, same stores).
 // Every wait is bounded (2 s of global time); a wait that runs out records an
 // error code in *err and the CTA leaves after its own copies have landed.
 #pragma once
@@ -201,6 +203,29 @@ __device__ __forceinline__ void stage_vectors(Stage<N, ROWS, LMAX>& s, const KPa
   }
 }
 
+// Slot resolution of one item, written by the producer for the consumers.
+struct __align__(16) SlotRec {
+  int64_t src, dst;
+  int read_ok, pad_;
+};
+
+// Slots of item `idx` (the producer's part of resolve_*: everything the copy
+// and the consumers need beyond the item's position).
+template <bool VARLEN, int ROWS>
+__device__ __forceinline__ SlotRec resolve_slots(const KParams& p, const OneTokenArgs& oa,
+                                                 const VarlenArgs& va, int64_t idx, int* p0,
+                                                 int* h) {
+  const Item it = resolve_item<VARLEN, ROWS>(p, oa, va, idx);
+  *p0 = it.p0;
+  *h = it.h;
+  SlotRec r;
+  r.src = it.src;
+  r.dst = it.dst;
+  r.read_ok = it.read_ok;
+  r.pad_ = 0;
+  return r;
+}
+
 template <class ST, class IT, int N, int WARPS, int UNR, int S, int LMAX>
 struct BulkConfig {
   using L = RowLayout<ST, N>;
@@ -209,8 +234,9 @@ struct BulkConfig {
   static constexpr int THREADS = CONSUMERS + 32;  // + one producer warp
   static constexpr int STAGE_BYTES = ROWS * N * (int)sizeof(ST);
   using Vec = Stage<N, ROWS, LMAX>;
-  static constexpr int VEC_OFF = S * STAGE_BYTES;
-  static constexpr int BAR_OFF = VEC_OFF + S * (int)sizeof(Vec);
+  static constexpr int VEC_OFF = S * STAGE_BYTES;               // two vector buffers
+  static constexpr int REC_OFF = VEC_OFF + 2 * (int)sizeof(Vec);  // S slot records
+  static constexpr int BAR_OFF = REC_OFF + S * (int)sizeof(SlotRec);
   static constexpr int SMEM = BAR_OFF + 2 * S * 8;
   static_assert(STAGE_BYTES % 16 == 0 && sizeof(Vec) % 16 == 0, "16-byte stage alignment");
 };
@@ -226,6 +252,7 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* bufs = smem;
   Vec* vecs = reinterpret_cast<Vec*>(smem + Cfg::VEC_OFF);
+  SlotRec* recs = reinterpret_cast<SlotRec*>(smem + Cfg::REC_OFF);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFF);
   uint64_t* empty = full + S;
   __shared__ int s_abort;
@@ -235,7 +262,7 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 2);        // producer: copy armed + vectors staged
+      mbar_init(&full[s], 1);        // the producer's arrival (with the copy's bytes)
       mbar_init(&empty[s], WARPS);   // one arrival per consumer warp
       s_issued[s] = -1;
     }
@@ -243,48 +270,37 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-
   const int64_t block_elems = (int64_t)p.P * N;
 
   if (warp == WARPS) {
-    // ---------------- producer warp ----------------
-    int64_t k = 0;
-    for (int64_t idx = blockIdx.x; idx < nitems; idx += gridDim.x, ++k) {
+    // ---------------- producer: one thread resolves slots and issues copies ----------------
+    if (lane != 0) return;
+    int64_t idx = blockIdx.x;
+    if (idx >= nitems) return;
+    int p0, h;
+    SlotRec next = resolve_slots<VARLEN, ROWS>(p, oa, va, idx, &p0, &h);
+    for (int64_t k = 0; idx < nitems; idx += gridDim.x, ++k) {
+      const SlotRec cur = next;
+      const int cur_p0 = p0, cur_h = h;
+      if (idx + gridDim.x < nitems)  // prefetch the next item's slots
+        next = resolve_slots<VARLEN, ROWS>(p, oa, va, idx + gridDim.x, &p0, &h);
       const int s = (int)(k % S);
       const uint32_t round = (uint32_t)(k / S);
       if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1)) {
-        if (lane == 0) atomicOr(err, kErrEmptyTimeout);
+        atomicOr(err, kErrEmptyTimeout);
         break;
       }
-      const Item it = resolve_item<VARLEN, ROWS>(p, oa, va, idx);
-      const int nrows = min(ROWS, p.P - it.p0);
-      if (lane == 0) {
-        if (it.read_ok) {
-          const uint32_t bytes = (uint32_t)(nrows * N * (int)sizeof(ST));
-          const ST* src = static_cast<const ST*>(p.state) +
-                          ((it.src * p.H + it.h) * block_elems + (int64_t)it.p0 * N);
-          mbar_arrive_expect_tx(&full[s], bytes);
-          bulk_load(bufs + (size_t)s * Cfg::STAGE_BYTES, src, bytes, &full[s]);
-          s_issued[s] = (int)round;
-        } else {
-          mbar_arrive(&full[s]);
-        }
-      }
-      if (it.len > 0)
-        stage_vectors<IT, N, ROWS, LMAX>(vecs[s], p, it, 0, min(it.len, LMAX), lane, 32);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[s]);
-    }
-    // Every copy issued above is consumed (and waited for) by the consumers
-    // before the CTA can finish, except after an abort: then make sure no
-    // copy is still writing into this CTA's shared memory.
-    if (lane == 0 && atomicAdd(&s_abort, 0) != 0) {
-      for (int s = 0; s < S; ++s) {
-        if (s_issued[s] < 0) continue;
-        const uint64_t t0 = global_ns();
-        while (!mbar_test(&full[s], (uint32_t)s_issued[s] & 1) &&
-               global_ns() - t0 < kWaitLimitNs) {
-        }
+      recs[s] = cur;
+      if (cur.read_ok) {
+        const int nrows = min(ROWS, p.P - cur_p0);
+        const uint32_t bytes = (uint32_t)(nrows * N * (int)sizeof(ST));
+        const ST* src = static_cast<const ST*>(p.state) +
+                        ((cur.src * p.H + cur_h) * block_elems + (int64_t)cur_p0 * N);
+        s_issued[s] = (int)round;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_load(bufs + (size_t)s * Cfg::STAGE_BYTES, src, bytes, &full[s]);
+      } else {
+        mbar_arrive(&full[s]);
       }
     }
     return;
@@ -301,21 +317,56 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
   for (int64_t idx = blockIdx.x; idx < nitems; idx += gridDim.x, ++k) {
     const int s = (int)(k % S);
     const uint32_t round = (uint32_t)(k / S);
-    const Item it = resolve_item<VARLEN, ROWS>(p, oa, va, idx);
-    const bool ok = mbar_wait(&full[s], round & 1);
-    if (!ok) s_abort = 1;
+    Vec& stg = vecs[k & 1];
+    // the item's position (no slot loads: the producer resolves those)
+    Item it;
+    {
+      const int tile = (int)(idx % p.tiles);
+      const int64_t rest = idx / p.tiles;
+      it.h = (int)(rest % p.H);
+      it.seq = rest / p.H;
+      it.p0 = tile * ROWS;
+      if constexpr (VARLEN) {
+        int64_t begin, end;
+        if (va.cu) {
+          begin = load_int(va.cu, it.seq, va.meta64);
+          end = load_int(va.cu, it.seq + 1, va.meta64);
+        } else {
+          begin = it.seq * va.dense_steps;
+          end = begin + va.dense_steps;
+        }
+        if (begin < 0) begin = 0;
+        if (end > va.rows) end = va.rows;
+        it.r0 = begin;
+        it.len = end > begin ? (int)(end - begin) : 0;
+      } else {
+        it.r0 = it.seq;
+        it.len = 1;
+      }
+    }
+    // stage this item's first steps (one round of loads) while its copy lands
+    if (it.len > 0)
+      stage_vectors<IT, N, ROWS, LMAX>(stg, p, it, 0, min(it.len, LMAX), ctid, Cfg::CONSUMERS);
+    if (!mbar_wait(&full[s], round & 1)) s_abort = 1;
     named_sync(1, Cfg::CONSUMERS);
     if (s_abort) {
-      if (ctid == 0) atomicOr(err, kErrFullTimeout);
+      if (ctid == 0) {
+        atomicOr(err, kErrFullTimeout);
+        for (int t = 0; t < S; ++t) {  // let this CTA's own copies land before leaving
+          const int r = *(volatile int*)&s_issued[t];
+          if (r < 0) continue;
+          const uint64_t t0 = global_ns();
+          while (!mbar_test(&full[t], (uint32_t)r & 1) && global_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
       return;
     }
-    if (it.len == 0) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      continue;
-    }
-    Vec& stg = vecs[s];
-    // state chunks of this thread's rows, widened to fp32
+    const SlotRec rec = recs[s];
+    it.src = rec.src;
+    it.dst = rec.dst;
+    it.read_ok = rec.read_ok != 0;
+    // state chunks of this thread's rows, widened to fp32; then release the stage
     float hs[UNR][L::EPL];
     const unsigned char* buf = bufs + (size_t)s * Cfg::STAGE_BYTES;
 #pragma unroll
@@ -331,6 +382,9 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
         Elem<ST>::unpack(raw, &hs[u][c * L::VEC]);
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+
     for (int t0 = 0; t0 < it.len; t0 += LMAX) {
       const int n = (it.len - t0) < LMAX ? (it.len - t0) : LMAX;
       if (t0 > 0) {
@@ -405,9 +459,6 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
         }
       }
     }
-    // release the stage (its state block and its vectors)
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
   }
 }
 

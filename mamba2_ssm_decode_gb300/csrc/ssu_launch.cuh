@@ -35,9 +35,12 @@ struct BulkTune {
   static constexpr int WARPS = T::WARPS;
   static constexpr int UNR = T::UNR;
   static constexpr int ROWS = WARPS * L::RPW * UNR;
-  static constexpr int PER_STAGE = ROWS * N * (int)sizeof(ST) + LMAX * (2 * N + 4 * ROWS) * 4;
-  static constexpr int BUDGET = 110 * 1024;  // two CTAs per SM
-  static constexpr int S = (4 * PER_STAGE <= BUDGET) ? 4 : (3 * PER_STAGE <= BUDGET) ? 3 : 2;
+  static constexpr int PER_STAGE = ROWS * N * (int)sizeof(ST);
+  static constexpr int FIXED = 2 * LMAX * (2 * N + 4 * ROWS) * 4;  // two vector buffers
+  static constexpr int BUDGET = 110 * 1024;                           // two CTAs per SM
+  static constexpr int S = (4 * PER_STAGE + FIXED <= BUDGET)   ? 4
+                           : (3 * PER_STAGE + FIXED <= BUDGET) ? 3
+                                                               : 2;
 };
 
 template <class ST, class IT, int N, bool VARLEN>
@@ -68,7 +71,7 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
                          int64_t nitems, cudaStream_t stream, int algorithm) {
   using T = Tune<ST, N>;
   using Cfg = SSUConfig<ST, IT, N, T::WARPS, T::UNR, T::LMAX>;
-  if (algorithm != 1 /* SSU_ALGO_DIRECT */) {
+  if (algorithm == 2 /* SSU_ALGO_BULK */) {
     const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
     const VarlenArgs v0 = va ? *va : VarlenArgs{};
     return varlen ? launch_bulk<ST, IT, N, true>(p, o0, v0, nitems, stream)

@@ -36,7 +36,11 @@ def run_gpu(case, out_dtype=None, algorithm="auto"):
         S, T = case.nseqs, case.dense_steps
 
         def d4(t):
-            return None if t is None else t.view(S, T, *t.shape[1:])
+            if t is None:
+                return None
+            if t.dim() == 2:   # per-head dt: [rows, H] -> [S, T, H, 1]
+                return t.view(S, T, t.shape[1], 1)
+            return t.view(S, T, *t.shape[1:])
 
         out = ssu.ssu_update_varlen(case.state, d4(case.x), d4(case.dt), case.A, d4(case.B),
                                     d4(case.C), num_accepted_tokens=case.num_accepted_tokens,
