@@ -421,9 +421,12 @@ def measure(name, device, seed, steps, warmup, stream, algorithm="auto"):
 # ---------------------------------------------------------------------------
 
 DEFAULT_WORKLOAD = "mamba2-2.7b-decode"
-EXTRAS = ["hybrid-grouped-decode", "mtp-varlen", "sweep-single-float32-b4096",
-          "sweep-single-bfloat16-b4096", "sweep-mtp-float32-b4096", "sweep-mtp-bfloat16-b4096",
-          "sweep-single-float32-b1024-nowrite"]
+EXTRAS = ["hybrid-grouped-decode", "mtp-varlen",
+          "sweep-single-float32-b1024", "sweep-single-bfloat16-b1024",
+          "sweep-mtp-float32-b1024", "sweep-mtp-bfloat16-b1024",
+          "sweep-single-float32-b4096", "sweep-single-bfloat16-b4096",
+          "sweep-mtp-float32-b4096", "sweep-mtp-bfloat16-b4096",
+          "sweep-single-float32-b1024-nowrite", "sweep-mtp-bfloat16-b1024-nowrite"]
 
 
 def dist_setup(n_gpus):

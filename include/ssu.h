@@ -64,8 +64,8 @@ typedef enum ssu_status {
  * Kernel selection (the pages' SSU entry points carry an `algorithm` choice
  * too: "ssu_dispatch" forwards MambaConfig.ssu_algorithm, "mate.mamba"
  * accepts auto/simple/vertical/horizontal and runs one kernel for all).
- *   SSU_ALGO_AUTO    the library's choice (currently DIRECT, the faster of the
- *                    two on every measured workload)
+ *   SSU_ALGO_AUTO    the library's choice: BULK for ssu_update, DIRECT for
+ *                    ssu_update_varlen (the faster of the two on each)
  *   SSU_ALGO_DIRECT  one CTA per (sequence, head, 64-row tile); each thread
  *                    loads its state chunks straight into registers
  *   SSU_ALGO_BULK    persistent CTAs; a producer warp streams each tile into a

@@ -161,7 +161,7 @@ __device__ __forceinline__ Item resolve_item(const KParams& p, const OneTokenArg
 }
 
 // Stage steps [t0, t0 + n) of an item with `nthr` threads numbered `tid`.
-template <class IT, int N, int ROWS, int LMAX>
+template <class ST, class IT, int N, int ROWS, int LMAX>
 __device__ __forceinline__ void stage_vectors(Stage<N, ROWS, LMAX>& s, const KParams& p,
                                               const Item& it, int t0, int n, int tid, int nthr) {
   const int g = it.h / p.hr;
@@ -170,8 +170,8 @@ __device__ __forceinline__ void stage_vectors(Stage<N, ROWS, LMAX>& s, const KPa
   for (int i = tid; i < n * N; i += nthr) {
     const int tt = i / N, k = i - tt * N;
     const int64_t r = it.r0 + t0 + tt;
-    s.B[tt][k] = io_to_float<IT>(Bp[r * p.B_rs + (int64_t)g * p.B_gs + k]);
-    s.C[tt][k] = io_to_float<IT>(Cp[r * p.C_rs + (int64_t)g * p.C_gs + k]);
+    s.B[tt][bc_slot<ST, N>(k)] = io_to_float<IT>(Bp[r * p.B_rs + (int64_t)g * p.B_gs + k]);
+    s.C[tt][bc_slot<ST, N>(k)] = io_to_float<IT>(Cp[r * p.C_rs + (int64_t)g * p.C_gs + k]);
   }
   const IT* xp = static_cast<const IT*>(p.x);
   const IT* zp = static_cast<const IT*>(p.z);
@@ -225,6 +225,94 @@ __device__ __forceinline__ SlotRec resolve_slots(const KParams& p, const OneToke
   r.pad_ = 0;
   return r;
 }
+
+// The per-step operands of one item, loaded into registers ahead of use:
+// thread `tid` of `NTHR` holds B/C values tid, tid + NTHR, ... of the item's
+// [n][2N] block and row values tid, tid + NTHR, ... of its [n][ROWS] block.
+template <class ST, class IT, int N, int ROWS, int LMAX, int NTHR>
+struct VecPrefetch {
+  static constexpr int BCPT = (LMAX * 2 * N + NTHR - 1) / NTHR;
+  static constexpr int RPT = (LMAX * ROWS + NTHR - 1) / NTHR;
+  IT bc[BCPT];
+  IT x[RPT], z[RPT];
+  float dt[RPT], A[RPT], D[RPT], bias[RPT];
+  int n;  // staged steps (0: nothing)
+
+  // Issue the loads of steps [0, n) of item `it` (rows r0 ..).
+  __device__ __forceinline__ void issue(const KParams& p, const Item& it, int n_, int tid) {
+    n = n_;
+    const int g = it.h / p.hr;
+    const IT* Bp = static_cast<const IT*>(p.B);
+    const IT* Cp = static_cast<const IT*>(p.C);
+#pragma unroll
+    for (int i = 0; i < BCPT; ++i) {
+      const int e = tid + i * NTHR;
+      if (e < n * 2 * N) {
+        const int tt = e / (2 * N), k = e - tt * 2 * N;
+        const int64_t r = it.r0 + tt;
+        bc[i] = k < N ? Bp[r * p.B_rs + (int64_t)g * p.B_gs + k]
+                      : Cp[r * p.C_rs + (int64_t)g * p.C_gs + (k - N)];
+      }
+    }
+    const IT* xp = static_cast<const IT*>(p.x);
+    const IT* zp = static_cast<const IT*>(p.z);
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int e = tid + i * NTHR;
+      const int tt = e / ROWS, j = e - tt * ROWS;
+      const int prow = it.p0 + j;
+      if (e < n * ROWS && prow < p.P) {
+        const int64_t r = it.r0 + tt;
+        x[i] = xp[r * p.x_rs + (int64_t)it.h * p.x_hs + prow];
+        if (zp) z[i] = zp[r * p.z_rs + (int64_t)it.h * p.z_hs + prow];
+        dt[i] = p.dt[r * p.dt_rs + (int64_t)it.h * p.dt_hs + (int64_t)prow * p.dt_ds];
+        A[i] = p.A[(int64_t)it.h * p.A_s + (int64_t)prow * p.A_ds];
+        D[i] = p.D ? p.D[(int64_t)it.h * p.D_s + (int64_t)prow * p.D_ds] : 0.0f;
+        bias[i] = p.dt_bias ? p.dt_bias[(int64_t)it.h * p.bias_s + (int64_t)prow * p.bias_ds]
+                            : 0.0f;
+      }
+    }
+  }
+
+  // Convert and write the loaded values into a staging buffer (the same
+  // values stage_vectors computes).
+  __device__ __forceinline__ void commit(Stage<N, ROWS, LMAX>& s, const KParams& p, int p0,
+                                         int tid) const {
+#pragma unroll
+    for (int i = 0; i < BCPT; ++i) {
+      const int e = tid + i * NTHR;
+      if (e < n * 2 * N) {
+        const int tt = e / (2 * N), k = e - tt * 2 * N;
+        if (k < N) s.B[tt][bc_slot<ST, N>(k)] = io_to_float<IT>(bc[i]);
+        else s.C[tt][bc_slot<ST, N>(k - N)] = io_to_float<IT>(bc[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int e = tid + i * NTHR;
+      if (e < n * ROWS) {
+        const int tt = e / ROWS, j = e - tt * ROWS;
+        float dA = 1.0f, dtx = 0.0f, Dx = 0.0f, gate = 1.0f;
+        if (p0 + j < p.P) {
+          const float xv = io_to_float<IT>(x[i]);
+          float dtv = dt[i] + bias[i];
+          if (p.softplus) dtv = softplus_f(dtv);
+          dA = expf(A[i] * dtv);
+          dtx = dtv * xv;
+          Dx = D[i] * xv;
+          if (p.z) {
+            const float zv = io_to_float<IT>(z[i]);
+            gate = zv / (1.0f + expf(-zv));
+          }
+        }
+        s.dA[tt][j] = dA;
+        s.dtx[tt][j] = dtx;
+        s.Dx[tt][j] = Dx;
+        s.gate[tt][j] = gate;
+      }
+    }
+  }
+};
 
 template <class ST, class IT, int N, int WARPS, int UNR, int S, int LMAX>
 struct BulkConfig {
@@ -310,45 +398,67 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
   const int q = lane % L::LPR;
   const int rr = lane / L::LPR;
   ST* state = static_cast<ST*>(p.state);
-  IT* out_io = static_cast<IT*>(p.out);
-  float* out_f = static_cast<float*>(p.out);
   const int ctid = threadIdx.x;  // 0 .. CONSUMERS-1
+
+  // the position of item idx (no slot loads: the producer resolves those);
+  // for the packed route `cu0` / `cu1` are the sequence's cu_seqlens entries
+  auto position = [&](int64_t idx, int64_t cu0, int64_t cu1) {
+    Item it;
+    const int tile = (int)(idx % p.tiles);
+    const int64_t rest = idx / p.tiles;
+    it.h = (int)(rest % p.H);
+    it.seq = rest / p.H;
+    it.p0 = tile * ROWS;
+    if constexpr (VARLEN) {
+      int64_t begin = cu0, end = cu1;
+      if (begin < 0) begin = 0;
+      if (end > va.rows) end = va.rows;
+      it.r0 = begin;
+      it.len = end > begin ? (int)(end - begin) : 0;
+    } else {
+      it.r0 = it.seq;
+      it.len = 1;
+    }
+    it.src = it.dst = -1;
+    it.read_ok = false;
+    return it;
+  };
+  auto seq_bounds = [&](int64_t idx, int64_t* cu0, int64_t* cu1) {
+    if constexpr (VARLEN) {
+      const int64_t seq = idx / p.tiles / p.H;
+      if (va.cu) {
+        *cu0 = load_int(va.cu, seq, va.meta64);
+        *cu1 = load_int(va.cu, seq + 1, va.meta64);
+      } else {
+        *cu0 = seq * va.dense_steps;
+        *cu1 = *cu0 + va.dense_steps;
+      }
+    } else {
+      *cu0 = *cu1 = 0;
+    }
+  };
+
+  VecPrefetch<ST, IT, N, ROWS, LMAX, Cfg::CONSUMERS> pf;
+  int64_t idx = blockIdx.x;
+  Item it_next;
+  if (idx < nitems) {  // prologue: the first item's operands
+    int64_t c0, c1;
+    seq_bounds(idx, &c0, &c1);
+    it_next = position(idx, c0, c1);
+    pf.issue(p, it_next, min(it_next.len, LMAX), ctid);
+    pf.commit(vecs[0], p, it_next.p0, ctid);
+  }
   int64_t k = 0;
-  for (int64_t idx = blockIdx.x; idx < nitems; idx += gridDim.x, ++k) {
+  for (; idx < nitems; idx += gridDim.x, ++k) {
     const int s = (int)(k % S);
     const uint32_t round = (uint32_t)(k / S);
     Vec& stg = vecs[k & 1];
-    // the item's position (no slot loads: the producer resolves those)
-    Item it;
-    {
-      const int tile = (int)(idx % p.tiles);
-      const int64_t rest = idx / p.tiles;
-      it.h = (int)(rest % p.H);
-      it.seq = rest / p.H;
-      it.p0 = tile * ROWS;
-      if constexpr (VARLEN) {
-        int64_t begin, end;
-        if (va.cu) {
-          begin = load_int(va.cu, it.seq, va.meta64);
-          end = load_int(va.cu, it.seq + 1, va.meta64);
-        } else {
-          begin = it.seq * va.dense_steps;
-          end = begin + va.dense_steps;
-        }
-        if (begin < 0) begin = 0;
-        if (end > va.rows) end = va.rows;
-        it.r0 = begin;
-        it.len = end > begin ? (int)(end - begin) : 0;
-      } else {
-        it.r0 = it.seq;
-        it.len = 1;
-      }
-    }
-    // stage this item's first steps (one round of loads) while its copy lands
-    if (it.len > 0)
-      stage_vectors<IT, N, ROWS, LMAX>(stg, p, it, 0, min(it.len, LMAX), ctid, Cfg::CONSUMERS);
+    Item it = it_next;
+    const int64_t nidx = idx + gridDim.x;
+    int64_t nc0 = 0, nc1 = 0;
+    if (nidx < nitems) seq_bounds(nidx, &nc0, &nc1);  // in flight during the wait
     if (!mbar_wait(&full[s], round & 1)) s_abort = 1;
-    named_sync(1, Cfg::CONSUMERS);
+    named_sync(1, Cfg::CONSUMERS);  // also publishes stg (committed last iteration)
     if (s_abort) {
       if (ctid == 0) {
         atomicOr(err, kErrFullTimeout);
@@ -367,7 +477,7 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
     it.dst = rec.dst;
     it.read_ok = rec.read_ok != 0;
     // state chunks of this thread's rows, widened to fp32; then release the stage
-    float hs[UNR][L::EPL];
+    float2 hs[UNR][L::EPL / 2];
     const unsigned char* buf = bufs + (size_t)s * Cfg::STAGE_BYTES;
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
@@ -379,73 +489,57 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
             rd ? *reinterpret_cast<const uint4*>(buf + ((size_t)j * N + (q + c * L::LPR) * L::VEC) *
                                                            sizeof(ST))
                : make_uint4(0u, 0u, 0u, 0u);
-        Elem<ST>::unpack(raw, &hs[u][c * L::VEC]);
+        Elem<ST>::unpack2(raw, &hs[u][c * L::VEC / 2]);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+    // the next item's operands: loads in flight while this item computes
+    if (nidx < nitems) {
+      it_next = position(nidx, nc0, nc1);
+      pf.issue(p, it_next, min(it_next.len, LMAX), ctid);
+    }
 
     for (int t0 = 0; t0 < it.len; t0 += LMAX) {
       const int n = (it.len - t0) < LMAX ? (it.len - t0) : LMAX;
       if (t0 > 0) {
         named_sync(1, Cfg::CONSUMERS);
-        stage_vectors<IT, N, ROWS, LMAX>(stg, p, it, t0, n, ctid, Cfg::CONSUMERS);
+        stage_vectors<ST, IT, N, ROWS, LMAX>(stg, p, it, t0, n, ctid, Cfg::CONSUMERS);
         named_sync(1, Cfg::CONSUMERS);
       }
-      for (int tt = 0; tt < n; ++tt) {
-        const int64_t r = it.r0 + t0 + tt;
-        float bv[L::EPL], cv[L::EPL];
+      // this chunk's write slots, loaded together ahead of the stores
+      int64_t dsts[LMAX];
+      bool dok[LMAX];
 #pragma unroll
-        for (int c = 0; c < L::CPL; ++c) {
-          const int k0 = (q + c * L::LPR) * L::VEC;
-#pragma unroll
-          for (int e = 0; e < L::VEC; e += 4) {
-            const float4 b4 = *reinterpret_cast<const float4*>(&stg.B[tt][k0 + e]);
-            const float4 c4 = *reinterpret_cast<const float4*>(&stg.C[tt][k0 + e]);
-            bv[c * L::VEC + e + 0] = b4.x; bv[c * L::VEC + e + 1] = b4.y;
-            bv[c * L::VEC + e + 2] = b4.z; bv[c * L::VEC + e + 3] = b4.w;
-            cv[c * L::VEC + e + 0] = c4.x; cv[c * L::VEC + e + 1] = c4.y;
-            cv[c * L::VEC + e + 2] = c4.z; cv[c * L::VEC + e + 3] = c4.w;
+      for (int i = 0; i < LMAX; ++i) {
+        dsts[i] = -1;
+        dok[i] = false;
+        if (i < n) {
+          if constexpr (VARLEN) {
+            const TableArgs dtab = va.dst.idx ? va.dst : va.src;
+            if (dtab.idx) {
+              int64_t v = -1;
+              dok[i] = table_entry(dtab, it.seq, t0 + i, va.idx64, &v);
+              dsts[i] = v;
+            } else {
+              dsts[i] = it.seq;
+              dok[i] = true;
+            }
+          } else {
+            dsts[i] = it.dst;
+            dok[i] = true;
           }
+          dok[i] = dok[i] && it.read_ok && !p.disable && slot_ok(dsts[i], p.pad, p.slots);
         }
+      }
 #pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-          const int j = (warp * UNR + u) * L::RPW + rr;
-          const float dA = stg.dA[tt][j];
-          const float dtx = stg.dtx[tt][j];
-          float acc0 = 0.0f, acc1 = 0.0f;
-#pragma unroll
-          for (int e = 0; e < L::EPL; ++e) {
-            const float hv = fmaf(hs[u][e], dA, dtx * bv[e]);
-            hs[u][e] = hv;
-            if (e & 1) acc1 = fmaf(hv, cv[e], acc1);
-            else acc0 = fmaf(hv, cv[e], acc0);
-          }
-          float acc = acc0 + acc1;
-#pragma unroll
-          for (int off = L::LPR / 2; off > 0; off >>= 1)
-            acc += __shfl_xor_sync(0xffffffffu, acc, off);
-          const int prow = it.p0 + j;
-          if (q == 0 && prow < p.P) {
-            const float yv = (acc + stg.Dx[tt][j]) * stg.gate[tt][j];
-            const int64_t o = r * p.o_rs + (int64_t)it.h * p.o_hs + prow;
-            if (p.out_f32) out_f[o] = yv;
-            else out_io[o] = float_to_io<IT>(yv);
-          }
-        }
+      for (int tt = 0; tt < LMAX; ++tt) {
+        if (tt >= n) break;
+        step_rows<ST, IT, N, UNR>(hs, stg, tt, q, warp * UNR * L::RPW + rr, p, it.h, it.p0,
+                                  it.r0 + t0 + tt);
         // this step's state
-        int64_t dst = -1;
-        bool have;
-        if constexpr (VARLEN) {
-          const TableArgs dtab = va.dst.idx ? va.dst : va.src;
-          if (dtab.idx) have = table_entry(dtab, it.seq, t0 + tt, va.idx64, &dst);
-          else { dst = it.seq; have = true; }
-        } else {
-          dst = it.dst;
-          have = true;
-        }
-        if (it.read_ok && !p.disable && have && slot_ok(dst, p.pad, p.slots)) {
-          ST* base = state + ((dst * p.H + it.h) * block_elems);
+        if (dok[tt]) {
+          ST* base = state + ((dsts[tt] * p.H + it.h) * block_elems);
 #pragma unroll
           for (int u = 0; u < UNR; ++u) {
             const int prow = it.p0 + (warp * UNR + u) * L::RPW + rr;
@@ -453,12 +547,15 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
 #pragma unroll
               for (int c = 0; c < L::CPL; ++c)
                 st_state(base + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
-                         Elem<ST>::pack(&hs[u][c * L::VEC]));
+                         Elem<ST>::pack2(&hs[u][c * L::VEC / 2]));
             }
           }
         }
       }
     }
+    // publish the next item's operands (every consumer left vecs[(k + 1) & 1]
+    // behind when it passed this item's barrier)
+    if (nidx < nitems) pf.commit(vecs[(k + 1) & 1], p, it_next.p0, ctid);
   }
 }
 

@@ -95,34 +95,30 @@ struct Elem;
 template <>
 struct Elem<float> {
   static constexpr int VEC = 4;  // elements per 16-byte chunk
-  __device__ static __forceinline__ void unpack(const uint4& r, float* f) {
-    f[0] = __uint_as_float(r.x);
-    f[1] = __uint_as_float(r.y);
-    f[2] = __uint_as_float(r.z);
-    f[3] = __uint_as_float(r.w);
+  __device__ static __forceinline__ void unpack2(const uint4& r, float2* f) {
+    f[0] = make_float2(__uint_as_float(r.x), __uint_as_float(r.y));
+    f[1] = make_float2(__uint_as_float(r.z), __uint_as_float(r.w));
   }
-  __device__ static __forceinline__ uint4 pack(const float* f) {
-    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
-                      __float_as_uint(f[3]));
+  __device__ static __forceinline__ uint4 pack2(const float2* f) {
+    return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                      __float_as_uint(f[1].y));
   }
 };
 
 template <>
 struct Elem<__nv_bfloat16> {
   static constexpr int VEC = 8;
-  __device__ static __forceinline__ void unpack(const uint4& r, float* f) {
+  __device__ static __forceinline__ void unpack2(const uint4& r, float2* f) {
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = __uint_as_float(w[i] << 16);              // element 2i: low half
-      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);  // element 2i+1: high half
-    }
+    for (int i = 0; i < 4; ++i)  // element 2i in the low half, 2i+1 in the high half
+      f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
   }
-  __device__ static __forceinline__ uint4 pack(const float* f) {
+  __device__ static __forceinline__ uint4 pack2(const float2* f) {
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 v = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);  // .x low, .y high
+      __nv_bfloat162 v = __float22bfloat162_rn(f[i]);  // .x low, .y high, round to nearest even
       w[i] = *reinterpret_cast<uint32_t*>(&v);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
@@ -132,21 +128,16 @@ struct Elem<__nv_bfloat16> {
 template <>
 struct Elem<__half> {
   static constexpr int VEC = 8;
-  __device__ static __forceinline__ void unpack(const uint4& r, float* f) {
+  __device__ static __forceinline__ void unpack2(const uint4& r, float2* f) {
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __half2 h2 = *reinterpret_cast<const __half2*>(&w[i]);
-      float2 v = __half22float2(h2);
-      f[2 * i] = v.x;
-      f[2 * i + 1] = v.y;
-    }
+    for (int i = 0; i < 4; ++i) f[i] = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
   }
-  __device__ static __forceinline__ uint4 pack(const float* f) {
+  __device__ static __forceinline__ uint4 pack2(const float2* f) {
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      __half2 v = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+      __half2 v = __float22half2_rn(f[i]);
       w[i] = *reinterpret_cast<uint32_t*>(&v);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
@@ -188,6 +179,122 @@ struct RowLayout {
   static constexpr int EPL = CPL * VEC;                 // elements per lane per row
   static_assert(CHUNKS % LPR == 0 && 32 % LPR == 0, "unsupported dstate");
 };
+
+// Position of state column k in a staged fp32 row of B or C.  Lane q of a
+// row reads its chunk c as VEC/4 float4 groups; group h of that chunk is
+// stored at ((c * VEC/4 + h) * LPR + q) * 4, so the 8 lanes of a quarter-warp
+// read 128 consecutive bytes (no bank conflicts) for every state dtype.  For
+// fp32 state (VEC 4) this is the identity.
+template <class ST, int N>
+__device__ __forceinline__ int bc_slot(int k) {
+  using L = RowLayout<ST, N>;
+  constexpr int H4 = L::VEC / 4;
+  const int chunk = k / L::VEC;
+  const int q = chunk % L::LPR, c = chunk / L::LPR;
+  const int h = (k % L::VEC) / 4;
+  return ((c * H4 + h) * L::LPR + q) * 4 + (k & 3);
+}
+
+// Load lane q's B and C values of step tt from the staged rows, as pairs
+// (pair e2 holds the lane's elements 2 e2 and 2 e2 + 1).
+template <class ST, int N, class StageT>
+__device__ __forceinline__ void lane_bc(const StageT& stg, int tt, int q, float2* bv, float2* cv) {
+  using L = RowLayout<ST, N>;
+  constexpr int H4 = L::VEC / 4;
+#pragma unroll
+  for (int c = 0; c < L::CPL; ++c) {
+#pragma unroll
+    for (int h = 0; h < H4; ++h) {
+      const int o = ((c * H4 + h) * L::LPR + q) * 4;
+      const float4 b4 = *reinterpret_cast<const float4*>(&stg.B[tt][o]);
+      const float4 c4 = *reinterpret_cast<const float4*>(&stg.C[tt][o]);
+      const int e2 = (c * L::VEC + 4 * h) / 2;
+      bv[e2] = make_float2(b4.x, b4.y);
+      bv[e2 + 1] = make_float2(b4.z, b4.w);
+      cv[e2] = make_float2(c4.x, c4.y);
+      cv[e2 + 1] = make_float2(c4.z, c4.w);
+    }
+  }
+}
+
+// Reduce-scatter of R per-row partial sums over the lanes of a row group:
+// at each offset (from LPR/2 down) a lane keeps half of its rows and sends
+// the other half to its partner, so after log2(R) exchanges every lane holds
+// one row summed over 2, 4, ... lanes; the remaining offsets are a plain
+// xor-reduction.  The sum of each row is formed in the same order as a plain
+// xor tree (own value + partner's value at each level).  On return the lane
+// owns rows [base, base + R_left) with their sums in v[0..R_left), and
+// `plain` holds the offsets of the plain levels (lanes with q & plain == 0
+// are the rows' unique owners).
+template <int R, int OFF>
+struct RowScatter {
+  __device__ static __forceinline__ void run(float* v, int q, int& base, int& plain) {
+    if constexpr (OFF > 0) {
+      if constexpr (R > 1) {
+        const bool upper = (q & OFF) != 0;
+#pragma unroll
+        for (int i = 0; i < R / 2; ++i) {
+          const float send = upper ? v[i] : v[R / 2 + i];
+          const float keep = upper ? v[R / 2 + i] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+        }
+        if (upper) base += R / 2;
+        RowScatter<R / 2, OFF / 2>::run(v, q, base, plain);
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], OFF);
+        plain |= OFF;
+        RowScatter<1, OFF / 2>::run(v, q, base, plain);
+      }
+    }
+  }
+};
+
+// One step of the recurrence for this thread's UNR state rows (pairs in hs):
+//   h <- h dA + (dt' x) B;  y = sum_n h C + D x;  y *= silu(z)
+// with the row's B, C, dA, dt' x, D x, silu(z) read from the staged step tt.
+// Rows of the tile are jbase + u * RPW (u < UNR); y goes to out row r.
+template <class ST, class IT, int N, int UNR, class StageT>
+__device__ __forceinline__ void step_rows(float2 (&hs)[UNR][RowLayout<ST, N>::EPL / 2],
+                                          const StageT& stg, int tt, int q, int jbase,
+                                          const KParams& p, int h, int p0, int64_t r) {
+  using L = RowLayout<ST, N>;
+  constexpr int E2 = L::EPL / 2;
+  float2 bv[E2], cv[E2];
+  lane_bc<ST, N>(stg, tt, q, bv, cv);
+  float acc[UNR];
+#pragma unroll
+  for (int u = 0; u < UNR; ++u) {
+    const int j = jbase + u * L::RPW;
+    const float dA = stg.dA[tt][j];
+    const float dtx = stg.dtx[tt][j];
+    const float2 dA2 = make_float2(dA, dA);
+    const float2 dtx2 = make_float2(dtx, dtx);
+    float2 a2 = make_float2(0.0f, 0.0f);  // even and odd elements: two partial sums
+#pragma unroll
+    for (int e2 = 0; e2 < E2; ++e2) {
+      const float2 hv = __ffma2_rn(hs[u][e2], dA2, __fmul2_rn(dtx2, bv[e2]));
+      hs[u][e2] = hv;
+      a2 = __ffma2_rn(hv, cv[e2], a2);
+    }
+    acc[u] = a2.x + a2.y;
+  }
+  int base = 0, plain = 0;
+  RowScatter<UNR, L::LPR / 2>::run(acc, q, base, plain);
+  constexpr int LEFT = UNR > L::LPR ? UNR / L::LPR : 1;  // rows a lane still owns
+  if ((q & plain) == 0) {
+#pragma unroll
+    for (int i = 0; i < LEFT; ++i) {
+      const int j = jbase + (base + i) * L::RPW;
+      const int prow = p0 + j;
+      if (prow < p.P) {
+        const float yv = (acc[i] + stg.Dx[tt][j]) * stg.gate[tt][j];
+        const int64_t o = r * p.o_rs + (int64_t)h * p.o_hs + prow;
+        if (p.out_f32) static_cast<float*>(p.out)[o] = yv;
+        else static_cast<IT*>(p.out)[o] = float_to_io<IT>(yv);
+      }
+    }
+  }
+}
 
 // ---------------------------------------------------------------------------
 // small helpers
@@ -247,7 +354,7 @@ struct __align__(16) Stage {
 };
 
 // Stage steps [t0, t0 + n) of rows [r0 + t0, ...) for head h / group g.
-template <class IT, int N, int ROWS, int LMAX, int THREADS>
+template <class ST, class IT, int N, int ROWS, int LMAX, int THREADS>
 __device__ __forceinline__ void stage_steps(Stage<N, ROWS, LMAX>& s, const KParams& p,
                                             int64_t r0, int t0, int n, int h, int g, int p0) {
   const IT* Bp = static_cast<const IT*>(p.B);
@@ -256,8 +363,8 @@ __device__ __forceinline__ void stage_steps(Stage<N, ROWS, LMAX>& s, const KPara
   for (int i = threadIdx.x; i < n * N; i += THREADS) {
     const int tt = i / N, k = i - tt * N;
     const int64_t r = r0 + t0 + tt;
-    s.B[tt][k] = io_to_float<IT>(Bp[r * p.B_rs + (int64_t)g * p.B_gs + k]);
-    s.C[tt][k] = io_to_float<IT>(Cp[r * p.C_rs + (int64_t)g * p.C_gs + k]);
+    s.B[tt][bc_slot<ST, N>(k)] = io_to_float<IT>(Bp[r * p.B_rs + (int64_t)g * p.B_gs + k]);
+    s.C[tt][bc_slot<ST, N>(k)] = io_to_float<IT>(Cp[r * p.C_rs + (int64_t)g * p.C_gs + k]);
   }
   // per-row scalars
   const IT* xp = static_cast<const IT*>(p.x);
@@ -327,72 +434,40 @@ __device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64
 
   // 2. stage the first steps while the loads are in flight
   int n0 = len < LMAX ? len : LMAX;
-  stage_steps<IT, N, ROWS, LMAX, THREADS>(stg, p, r0, 0, n0, h, g, p0);
+  stage_steps<ST, IT, N, ROWS, LMAX, THREADS>(stg, p, r0, 0, n0, h, g, p0);
   __syncthreads();
 
   // 3. widen the state to fp32 registers
-  float hs[UNR][L::EPL];
+  float2 hs[UNR][L::EPL / 2];
 #pragma unroll
   for (int u = 0; u < UNR; ++u)
 #pragma unroll
-    for (int c = 0; c < L::CPL; ++c) Elem<ST>::unpack(raw[u][c], &hs[u][c * L::VEC]);
-
-  IT* out_io = static_cast<IT*>(p.out);
-  float* out_f = static_cast<float*>(p.out);
+    for (int c = 0; c < L::CPL; ++c) Elem<ST>::unpack2(raw[u][c], &hs[u][c * L::VEC / 2]);
+  const int jbase = warp * UNR * L::RPW + rr;
 
   for (int t0 = 0; t0 < len; t0 += LMAX) {
     const int n = (len - t0) < LMAX ? (len - t0) : LMAX;
     if (t0 > 0) {
       __syncthreads();  // everyone is done with the previous stage
-      stage_steps<IT, N, ROWS, LMAX, THREADS>(stg, p, r0, t0, n, h, g, p0);
+      stage_steps<ST, IT, N, ROWS, LMAX, THREADS>(stg, p, r0, t0, n, h, g, p0);
       __syncthreads();
     }
-    for (int tt = 0; tt < n; ++tt) {
-      const int64_t r = r0 + t0 + tt;
-      // this lane's B and C values
-      float bv[L::EPL], cv[L::EPL];
+    // this chunk's write slots, loaded together ahead of the stores
+    int64_t dsts[LMAX];
+    bool dok[LMAX];
 #pragma unroll
-      for (int c = 0; c < L::CPL; ++c) {
-        const int k0 = (q + c * L::LPR) * L::VEC;
+    for (int i = 0; i < LMAX; ++i) {
+      int64_t v = -1;
+      dok[i] = i < n && read_ok && !p.disable && dst_of(t0 + i, &v) && slot_ok(v, p.pad, p.slots);
+      dsts[i] = v;
+    }
 #pragma unroll
-        for (int e = 0; e < L::VEC; e += 4) {
-          const float4 b4 = *reinterpret_cast<const float4*>(&stg.B[tt][k0 + e]);
-          const float4 c4 = *reinterpret_cast<const float4*>(&stg.C[tt][k0 + e]);
-          bv[c * L::VEC + e + 0] = b4.x; bv[c * L::VEC + e + 1] = b4.y;
-          bv[c * L::VEC + e + 2] = b4.z; bv[c * L::VEC + e + 3] = b4.w;
-          cv[c * L::VEC + e + 0] = c4.x; cv[c * L::VEC + e + 1] = c4.y;
-          cv[c * L::VEC + e + 2] = c4.z; cv[c * L::VEC + e + 3] = c4.w;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const int j = (warp * UNR + u) * L::RPW + rr;  // row within the CTA tile
-        const float dA = stg.dA[tt][j];
-        const float dtx = stg.dtx[tt][j];
-        float acc0 = 0.0f, acc1 = 0.0f;  // two partial sums: shorter rounding chains
-#pragma unroll
-        for (int e = 0; e < L::EPL; ++e) {
-          const float hv = fmaf(hs[u][e], dA, dtx * bv[e]);
-          hs[u][e] = hv;
-          if (e & 1) acc1 = fmaf(hv, cv[e], acc1);
-          else acc0 = fmaf(hv, cv[e], acc0);
-        }
-        float acc = acc0 + acc1;
-#pragma unroll
-        for (int off = L::LPR / 2; off > 0; off >>= 1)
-          acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        const int prow = p0 + j;
-        if (q == 0 && prow < p.P) {
-          const float yv = (acc + stg.Dx[tt][j]) * stg.gate[tt][j];
-          const int64_t o = r * p.o_rs + (int64_t)h * p.o_hs + prow;
-          if (p.out_f32) out_f[o] = yv;
-          else out_io[o] = float_to_io<IT>(yv);
-        }
-      }
+    for (int tt = 0; tt < LMAX; ++tt) {
+      if (tt >= n) break;
+      step_rows<ST, IT, N, UNR>(hs, stg, tt, q, jbase, p, h, p0, r0 + t0 + tt);
       // write this step's state
-      int64_t dst;
-      if (read_ok && !p.disable && dst_of(t0 + tt, &dst) && slot_ok(dst, p.pad, p.slots)) {
-        ST* base = state + ((dst * p.H + h) * block_elems);
+      if (dok[tt]) {
+        ST* base = state + ((dsts[tt] * p.H + h) * block_elems);
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
           const int prow = p0 + (warp * UNR + u) * L::RPW + rr;
@@ -400,7 +475,7 @@ __device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c)
               st_state(base + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
-                       Elem<ST>::pack(&hs[u][c * L::VEC]));
+                       Elem<ST>::pack2(&hs[u][c * L::VEC / 2]));
           }
         }
       }
@@ -410,7 +485,7 @@ __device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64
 
 // One-token decode: blockIdx -> (sequence b, head, row tile).
 template <class ST, class IT, int N, int WARPS, int UNR>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     ssu_one_token_kernel(const KParams p, const OneTokenArgs a) {
   int64_t bid = blockIdx.x;
   const int tile = (int)(bid % p.tiles);
@@ -429,7 +504,7 @@ __global__ void __launch_bounds__(WARPS * 32)
 
 // Packed varlen / MTP: blockIdx -> (sequence s, head, row tile).
 template <class ST, class IT, int N, int WARPS, int UNR, int LMAX>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     ssu_varlen_kernel(const KParams p, const VarlenArgs a) {
   int64_t bid = blockIdx.x;
   const int tile = (int)(bid % p.tiles);

@@ -25,35 +25,39 @@ struct Tune {
   static constexpr int LMAX = 4;
 };
 
-// Bulk-copy pipeline per (state dtype, dstate, staged steps): the same
-// 4-warp x 64-row consumer tile as Tune, plus a producer warp, with as many
-// shared-memory stages (2..4) as let two CTAs share an SM.
-template <class ST, int N, int LMAX>
+// Bulk-copy pipeline shape: CW consumer warps, each thread owning UNR state
+// rows (capped so a tile has at most 64 rows), plus one producer warp; as
+// many shared-memory stages (2..4) as fit the per-CTA budget (two CTAs per SM
+// for 32 KB tiles, three for 16 KB and smaller).
+template <class ST, int N, int LMAX, int CW, int UNR_>
 struct BulkTune {
-  using T = Tune<ST, N>;
-  using L = typename T::L;
-  static constexpr int WARPS = T::WARPS;
-  static constexpr int UNR = T::UNR;
+  using L = RowLayout<ST, N>;
+  static constexpr int WARPS = CW;
+  static constexpr int UNR = cmax(1, cmin(UNR_, cmax(1, 64 / (CW * L::RPW))));
   static constexpr int ROWS = WARPS * L::RPW * UNR;
   static constexpr int PER_STAGE = ROWS * N * (int)sizeof(ST);
   static constexpr int FIXED = 2 * LMAX * (2 * N + 4 * ROWS) * 4;  // two vector buffers
-  static constexpr int BUDGET = 110 * 1024;                           // two CTAs per SM
+  static constexpr int BUDGET = (PER_STAGE > 16 * 1024 ? 110 : 72) * 1024;
   static constexpr int S = (4 * PER_STAGE + FIXED <= BUDGET)   ? 4
                            : (3 * PER_STAGE + FIXED <= BUDGET) ? 3
                                                                : 2;
 };
 
-template <class ST, class IT, int N, bool VARLEN>
-cudaError_t launch_bulk(KParams p, const OneTokenArgs& oa, const VarlenArgs& va, int64_t nitems,
-                        cudaStream_t stream) {
+template <class ST, class IT, int N, bool VARLEN, int CW, int UNR_>
+cudaError_t launch_bulk_cfg(KParams p, const OneTokenArgs& oa, const VarlenArgs& va,
+                            int64_t nitems, cudaStream_t stream) {
   constexpr int LMAX = VARLEN ? Tune<ST, N>::LMAX : 1;
-  using BT = BulkTune<ST, N, LMAX>;
+  using BT = BulkTune<ST, N, LMAX, CW, UNR_>;
   using Cfg = BulkConfig<ST, IT, N, BT::WARPS, BT::UNR, BT::S, LMAX>;
   auto kern = ssu_bulk_kernel<ST, IT, N, BT::WARPS, BT::UNR, BT::S, LMAX, VARLEN>;
   p.tiles = (p.P + Cfg::ROWS - 1) / Cfg::ROWS;
   const int64_t items = nitems * (int64_t)p.H * p.tiles;
   if (items <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+  if (e != cudaSuccess) return e;
+  // all of the unified L1 / shared array as shared memory: several CTAs per SM
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Cfg::THREADS, Cfg::SMEM);
@@ -66,12 +70,26 @@ cudaError_t launch_bulk(KParams p, const OneTokenArgs& oa, const VarlenArgs& va,
   return cudaGetLastError();
 }
 
+// Tile per state dtype (measured): fp32 state streams best in 32-row tiles
+// (16 KB, four stages, three CTAs per SM), 16-bit state in 64-row tiles.
+template <class ST, class IT, int N, bool VARLEN>
+cudaError_t launch_bulk(KParams p, const OneTokenArgs& oa, const VarlenArgs& va, int64_t nitems,
+                        cudaStream_t stream) {
+  if constexpr (sizeof(ST) == 4)
+    return launch_bulk_cfg<ST, IT, N, VARLEN, 4, 2>(p, oa, va, nitems, stream);
+  else
+    return launch_bulk_cfg<ST, IT, N, VARLEN, 4, 4>(p, oa, va, nitems, stream);
+}
+
 template <class ST, class IT, int N>
 cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const VarlenArgs* va,
                          int64_t nitems, cudaStream_t stream, int algorithm) {
   using T = Tune<ST, N>;
   using Cfg = SSUConfig<ST, IT, N, T::WARPS, T::UNR, T::LMAX>;
-  if (algorithm == 2 /* SSU_ALGO_BULK */) {
+  // auto: the bulk-copy pipeline for one-token calls, the register kernel for
+  // multi-token chains (the faster of the two on each, as measured)
+  const bool bulk = algorithm == 2 /* SSU_ALGO_BULK */ || (algorithm == 0 && !varlen);
+  if (bulk) {
     const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
     const VarlenArgs v0 = va ? *va : VarlenArgs{};
     return varlen ? launch_bulk<ST, IT, N, true>(p, o0, v0, nitems, stream)
