@@ -271,6 +271,16 @@ ssu_status ssu_ring_commit(int32_t* ring_start, int64_t ring_start_len,
  */
 ssu_status ssu_device_error(unsigned int* value, int reset);
 
+/*
+ * Self-test of the bounded waits (no counterpart on the pages): launches, on
+ * the current device's legacy default stream, one CTA that waits on an
+ * mbarrier nothing completes; the wait must give up after limit_ns (0 <
+ * limit_ns <= 1e9), set bit 1 of the device error word and return, leaving the
+ * context usable.  *waited_ns receives the measured wait.  SYNCHRONISES the
+ * device.
+ */
+ssu_status ssu_selftest_bounded_wait(uint64_t limit_ns, uint64_t* waited_ns);
+
 /* Static description of a status code. */
 const char* ssu_status_string(ssu_status status);
 

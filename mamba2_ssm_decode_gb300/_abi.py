@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
         L.ssu_last_error.argtypes = []
         L.ssu_device_error.restype = _c_int
         L.ssu_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _c_int]
+        L.ssu_selftest_bounded_wait.restype = _c_int
+        L.ssu_selftest_bounded_wait.argtypes = [ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64)]
         L.ssu_abi_version.restype = _c_int
         L.ssu_abi_version.argtypes = []
         if L.ssu_abi_version() != ABI_VERSION:

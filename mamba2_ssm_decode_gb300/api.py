@@ -315,6 +315,14 @@ def ssu_device_error(reset=False):
     return v.value
 
 
+def ssu_selftest_bounded_wait(limit_ns):
+    """Run the bounded-wait self-test (C ABI ``ssu_selftest_bounded_wait``); returns
+    the nanoseconds the device waited before giving up.  Synchronises."""
+    v = ctypes.c_uint64(0)
+    _abi.check(_abi.lib().ssu_selftest_bounded_wait(int(limit_ns), ctypes.byref(v)))
+    return v.value
+
+
 def ssu_ring_update(ring_start, prev_num_accepted, prev_query_len, state_batch_indices,
                     logical_window=None, ring_buffer_len=None, pad_slot_id=-1, stream=None):
     """ReplaySSM tracker update (C ABI ``ssu_ring_update``); ``logical_window=None``

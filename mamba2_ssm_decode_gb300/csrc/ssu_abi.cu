@@ -19,6 +19,8 @@ constexpr int kMaxDevices = 64;
 
 // Error word of the bulk-copy kernels (one per device: module memory).
 __device__ unsigned int g_ssu_device_error = 0;
+// Duration the last bounded-wait self-test waited (module memory).
+__device__ unsigned long long g_ssu_selftest_waited_ns = 0;
 
 namespace ssu {
 
@@ -349,6 +351,23 @@ ssu_status ssu_device_error(unsigned int* value, int reset) {
   }
   if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "reading the error word failed: %s",
                                     cudaGetErrorString(e));
+  return ok();
+}
+
+ssu_status ssu_selftest_bounded_wait(uint64_t limit_ns, uint64_t* waited_ns) {
+  if (!waited_ns) return fail(SSU_ERR_INVALID_ARGUMENT, "waited_ns must not be NULL");
+  if (limit_ns == 0 || limit_ns > 1000000000ull)
+    return fail(SSU_ERR_INVALID_ARGUMENT, "limit_ns must be in (0, 1e9]");
+  void* w = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&w, g_ssu_selftest_waited_ns);
+  if (e == cudaSuccess)
+    e = ssu::launch_bounded_wait_probe(limit_ns, static_cast<unsigned long long*>(w), nullptr);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  unsigned long long v = 0;
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_ssu_selftest_waited_ns, sizeof v);
+  if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "bounded-wait self-test failed: %s",
+                                    cudaGetErrorString(e));
+  *waited_ns = v;
   return ok();
 }
 

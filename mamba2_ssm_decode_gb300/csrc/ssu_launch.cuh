@@ -71,14 +71,16 @@ cudaError_t launch_bulk_cfg(KParams p, const OneTokenArgs& oa, const VarlenArgs&
 }
 
 // Tile per state dtype (measured): fp32 state streams best in 32-row tiles
-// (16 KB, four stages, three CTAs per SM), 16-bit state in 64-row tiles.
+// (16 KB, four stages, three CTAs per SM) when it is written back, in 64-row
+// tiles when it is only read (half the bytes per unit of compute); 16-bit
+// state in 64-row tiles.
 template <class ST, class IT, int N, bool VARLEN>
 cudaError_t launch_bulk(KParams p, const OneTokenArgs& oa, const VarlenArgs& va, int64_t nitems,
                         cudaStream_t stream) {
-  if constexpr (sizeof(ST) == 4)
-    return launch_bulk_cfg<ST, IT, N, VARLEN, 4, 2>(p, oa, va, nitems, stream);
-  else
-    return launch_bulk_cfg<ST, IT, N, VARLEN, 4, 4>(p, oa, va, nitems, stream);
+  if constexpr (sizeof(ST) == 4) {
+    if (!p.disable) return launch_bulk_cfg<ST, IT, N, VARLEN, 4, 2>(p, oa, va, nitems, stream);
+  }
+  return launch_bulk_cfg<ST, IT, N, VARLEN, 4, 4>(p, oa, va, nitems, stream);
 }
 
 template <class ST, class IT, int N>
@@ -132,6 +134,10 @@ cudaError_t launch_state_bf16(int N, bool io_bf16, bool varlen, const KParams& p
 cudaError_t launch_state_f16(int N, bool io_bf16, bool varlen, const KParams& p,
                              const OneTokenArgs* oa, const VarlenArgs* va, int64_t nitems,
                              cudaStream_t stream, int algorithm);
+
+// defined in selftest.cu
+cudaError_t launch_bounded_wait_probe(uint64_t limit_ns, unsigned long long* waited_ns,
+                                      cudaStream_t stream);
 
 // defined in ring_trackers.cu
 cudaError_t launch_ring_update(int32_t* rs, int32_t* pna, int32_t* pql, const void* sbi,
