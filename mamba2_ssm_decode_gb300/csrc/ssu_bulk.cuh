@@ -318,8 +318,265 @@ struct VecPrefetch {
   }
 };
 
-template <class ST, class IT, int N, int WARPS, int UNR, int S, int LMAX>
+// What the producer publishes with each item (besides the tile and operands).
+template <int LMAX>
+struct __align__(16) ItemRec {
+  int64_t r0;           // first packed row
+  int64_t dst[LMAX];    // write slot of staged step t (valid where bit t of wmask is set)
+  int32_t h, p0, len;   // head, first tile row, rows of the sequence
+  int32_t read_ok;      // the tile holds the read slot's state (else zeros)
+  int32_t wmask;        // bit t: step t writes its state
+  int32_t pad_[3];
+};
+
+template <class ST, class IT, int N, int WARPS, int UNR, int S, int SV, int LMAX>
 struct BulkConfig {
+  using L = RowLayout<ST, N>;
+  static constexpr int ROWS = WARPS * L::RPW * UNR;
+  static constexpr int CONSUMERS = WARPS * 32;
+  static constexpr int THREADS = CONSUMERS + 32;  // + one producer warp
+  static constexpr int STAGE_BYTES = ROWS * N * (int)sizeof(ST);
+  using Vec = Stage<N, ROWS, LMAX>;
+  using Rec = ItemRec<LMAX>;
+  static constexpr int VEC_OFF = S * STAGE_BYTES;                  // SV operand buffers
+  static constexpr int REC_OFF = VEC_OFF + SV * (int)sizeof(Vec);  // S item records
+  static constexpr int BAR_OFF = REC_OFF + S * (int)sizeof(Rec);
+  static constexpr int SMEM = BAR_OFF + (2 * S + SV) * 8;
+  static_assert(STAGE_BYTES % 16 == 0 && sizeof(Vec) % 16 == 0, "16-byte stage alignment");
+};
+
+// The persistent pipeline.  Producer warp (32 lanes), for item k of this CTA:
+//   resolve the item (one item ahead: its index loads are in flight while the
+//   warp waits), wait until stage k % S is free, publish the item record and
+//   start the tile's bulk copy (first arrival on full[s], with the byte count),
+//   wait until operand buffer k % SV is free, convert the operands it loaded one
+//   item earlier into it, arrive on full[s] a second time, then issue the loads
+//   of the next item's operands.
+// Consumer warps: wait full[s], read the record and their rows of the tile,
+//   release the tile (empty_tile[s]) at once, run the steps on the buffered
+//   operands, release the operand buffer (empty_vec[v]).  They meet only for
+//   the rare chains longer than LMAX steps (re-staging the buffer).
+template <class ST, class IT, int N, int WARPS, int UNR, int S, int SV, int LMAX, bool VARLEN>
+__global__ void __launch_bounds__(WARPS * 32 + 32,
+                                  (WARPS * RowLayout<ST, N>::RPW * UNR * N * sizeof(ST) <= 16384)
+                                      ? 3
+                                      : 2)
+    ssu_bulk_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t nitems,
+                    unsigned* err) {
+  using Cfg = BulkConfig<ST, IT, N, WARPS, UNR, S, SV, LMAX>;
+  using L = typename Cfg::L;
+  using Vec = typename Cfg::Vec;
+  using Rec = typename Cfg::Rec;
+  constexpr int ROWS = Cfg::ROWS;
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* bufs = smem;
+  Vec* vring = reinterpret_cast<Vec*>(smem + Cfg::VEC_OFF);
+  Rec* recs = reinterpret_cast<Rec*>(smem + Cfg::REC_OFF);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFF);
+  uint64_t* empty_tile = full + S;
+  uint64_t* empty_vec = full + 2 * S;
+  __shared__ int s_issued[S];  // last round whose copy was issued on each stage (-1: none)
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 2);          // producer: record + copy armed; operands staged
+      mbar_init(&empty_tile[s], WARPS);
+      s_issued[s] = -1;
+    }
+    for (int v = 0; v < SV; ++v) mbar_init(&empty_vec[v], WARPS);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int64_t block_elems = (int64_t)p.P * N;
+
+  if (warp == WARPS) {
+    // ---------------------------- producer warp ----------------------------
+    int64_t idx = blockIdx.x;
+    if (idx >= nitems) return;
+    VecPrefetch<ST, IT, N, ROWS, LMAX, 32> pf;
+    Item cur = resolve_item<VARLEN, ROWS>(p, oa, va, idx);
+    pf.issue(p, cur, min(cur.len, LMAX), lane);
+    for (int64_t k = 0; idx < nitems; idx += gridDim.x, ++k) {
+      const int64_t nidx = idx + gridDim.x;
+      Item next;
+      if (nidx < nitems) next = resolve_item<VARLEN, ROWS>(p, oa, va, nidx);
+      const int s = (int)(k % S);
+      const int v = (int)(k % SV);
+      // the item record: write slots of the staged steps
+      Rec rec;
+      rec.r0 = cur.r0;
+      rec.h = cur.h;
+      rec.p0 = cur.p0;
+      rec.len = cur.len;
+      rec.read_ok = cur.read_ok;
+      rec.wmask = 0;
+#pragma unroll
+      for (int t = 0; t < LMAX; ++t) {
+        int64_t d = -1;
+        bool w = false;
+        if (t < cur.len && cur.read_ok && !p.disable) {
+          if constexpr (VARLEN) {
+            const TableArgs dtab = va.dst.idx ? va.dst : va.src;
+            if (dtab.idx) w = table_entry(dtab, cur.seq, t, va.idx64, &d);
+            else { d = cur.seq; w = true; }
+          } else {
+            d = cur.dst;
+            w = true;
+          }
+          w = w && slot_ok(d, p.pad, p.slots);
+        }
+        rec.dst[t] = d;
+        if (w) rec.wmask |= 1 << t;
+      }
+      if (k >= S && !mbar_wait(&empty_tile[s], (uint32_t)((k / S) - 1) & 1)) {
+        if (lane == 0) atomicOr(err, kErrEmptyTimeout);
+        break;
+      }
+      if (lane == 0) {
+        recs[s] = rec;
+        if (cur.read_ok) {
+          const int nrows = min(ROWS, p.P - cur.p0);
+          const uint32_t bytes = (uint32_t)(nrows * N * (int)sizeof(ST));
+          const ST* src = static_cast<const ST*>(p.state) +
+                          ((cur.src * p.H + cur.h) * block_elems + (int64_t)cur.p0 * N);
+          s_issued[s] = (int)(k / S);
+          mbar_arrive_expect_tx(&full[s], bytes);
+          bulk_load(bufs + (size_t)s * Cfg::STAGE_BYTES, src, bytes, &full[s]);
+        } else {
+          mbar_arrive(&full[s]);
+        }
+      }
+      if (k >= SV && !mbar_wait(&empty_vec[v], (uint32_t)((k / SV) - 1) & 1)) {
+        if (lane == 0) atomicOr(err, kErrEmptyTimeout);
+        break;
+      }
+      pf.commit(vring[v], p, cur.p0, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[s]);
+      if (nidx < nitems) {
+        pf.issue(p, next, min(next.len, LMAX), lane);
+        cur = next;
+      }
+    }
+    // after an abort, let the copies this CTA issued land before it leaves
+    if (lane == 0 && (*(volatile unsigned*)err & kErrEmptyTimeout)) {
+      for (int t = 0; t < S; ++t) {
+        const int r = *(volatile int*)&s_issued[t];
+        if (r < 0) continue;
+        const uint64_t t0 = global_ns();
+        while (!mbar_test(&full[t], (uint32_t)r & 1) && global_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------------------- consumer warps ----------------------------
+  const int q = lane % L::LPR;
+  const int rr = lane / L::LPR;
+  const int jbase = warp * UNR * L::RPW + rr;  // this thread's first row in a tile
+  ST* state = static_cast<ST*>(p.state);
+  int64_t k = 0;
+  for (int64_t idx = blockIdx.x; idx < nitems; idx += gridDim.x, ++k) {
+    const int s = (int)(k % S);
+    const int v = (int)(k % SV);
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (uint32_t)(k / S) & 1))) {
+      if (lane == 0) atomicOr(err, kErrFullTimeout);
+      return;
+    }
+    const Rec& rec = recs[s];
+    const int64_t r0 = rec.r0;
+    const int h = rec.h, p0 = rec.p0, len = rec.len, wmask = rec.wmask;
+    const bool read_ok = rec.read_ok != 0;
+    int64_t dsts[LMAX];
+#pragma unroll
+    for (int t = 0; t < LMAX; ++t) dsts[t] = rec.dst[t];
+    // this thread's rows of the tile, widened to fp32; then release the tile
+    float2 hs[UNR][L::EPL / 2];
+    const unsigned char* buf = bufs + (size_t)s * Cfg::STAGE_BYTES;
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int j = jbase + u * L::RPW;
+      const bool rd = read_ok && p0 + j < p.P;
+#pragma unroll
+      for (int c = 0; c < L::CPL; ++c) {
+        const uint4 raw =
+            rd ? *reinterpret_cast<const uint4*>(buf + ((size_t)j * N + (q + c * L::LPR) * L::VEC) *
+                                                           sizeof(ST))
+               : make_uint4(0u, 0u, 0u, 0u);
+        Elem<ST>::unpack2(raw, &hs[u][c * L::VEC / 2]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_tile[s]);
+
+    Vec& stg = vring[v];
+    for (int t0 = 0; t0 < len; t0 += LMAX) {
+      const int n = (len - t0) < LMAX ? (len - t0) : LMAX;
+      int wm = wmask;
+      if (t0 > 0) {
+        // a chain longer than LMAX: the consumers re-stage the buffer together
+        Item it;
+        it.h = h;
+        it.p0 = p0;
+        it.r0 = r0;
+        it.seq = idx / p.tiles / p.H;
+        named_sync(1, Cfg::CONSUMERS);
+        stage_vectors<ST, IT, N, ROWS, LMAX>(stg, p, it, t0, n, threadIdx.x, Cfg::CONSUMERS);
+        named_sync(1, Cfg::CONSUMERS);
+        wm = 0;
+#pragma unroll
+        for (int i = 0; i < LMAX; ++i) {
+          int64_t d = -1;
+          bool w = false;
+          if (i < n && read_ok && !p.disable) {
+            if constexpr (VARLEN) {
+              const TableArgs dtab = va.dst.idx ? va.dst : va.src;
+              if (dtab.idx) w = table_entry(dtab, it.seq, t0 + i, va.idx64, &d);
+              else { d = it.seq; w = true; }
+            }
+            w = w && slot_ok(d, p.pad, p.slots);
+          }
+          dsts[i] = d;
+          if (w) wm |= 1 << i;
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < LMAX; ++tt) {
+        if (tt >= n) break;
+        step_rows<ST, IT, N, UNR>(hs, stg, tt, q, jbase, p, h, p0, r0 + t0 + tt);
+        if ((wm >> tt) & 1) {
+          ST* base = state + ((dsts[tt] * p.H + h) * block_elems);
+#pragma unroll
+          for (int u = 0; u < UNR; ++u) {
+            const int prow = p0 + jbase + u * L::RPW;
+            if (prow < p.P) {
+#pragma unroll
+              for (int c = 0; c < L::CPL; ++c)
+                st_state(base + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
+                         Elem<ST>::pack2(&hs[u][c * L::VEC / 2]));
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_vec[v]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Variant with consumer-staged operands: the producer thread only resolves
+// slots and issues tile copies; the consumer warps stage each item's per-step
+// operands together (one round of loads, prefetched one item ahead, published
+// through a per-item named barrier of the consumer warps).  It wins where the
+// per-row operand work is large against the tile's bytes (16-bit state, calls
+// that write no state); the producer-staged kernel above wins elsewhere.
+// ---------------------------------------------------------------------------
+template <class ST, class IT, int N, int WARPS, int UNR, int S, int LMAX>
+struct BulkCsConfig {
   using L = RowLayout<ST, N>;
   static constexpr int ROWS = WARPS * L::RPW * UNR;
   static constexpr int CONSUMERS = WARPS * 32;
@@ -335,9 +592,9 @@ struct BulkConfig {
 
 template <class ST, class IT, int N, int WARPS, int UNR, int S, int LMAX, bool VARLEN>
 __global__ void __launch_bounds__(WARPS * 32 + 32)
-    ssu_bulk_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t nitems,
+    ssu_bulk_cs_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t nitems,
                     unsigned* err) {
-  using Cfg = BulkConfig<ST, IT, N, WARPS, UNR, S, LMAX>;
+  using Cfg = BulkCsConfig<ST, IT, N, WARPS, UNR, S, LMAX>;
   using L = typename Cfg::L;
   using Vec = typename Cfg::Vec;
   constexpr int ROWS = Cfg::ROWS;

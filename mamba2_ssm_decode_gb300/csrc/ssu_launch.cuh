@@ -27,8 +27,8 @@ struct Tune {
 
 // Bulk-copy pipeline shape: CW consumer warps, each thread owning UNR state
 // rows (capped so a tile has at most 64 rows), plus one producer warp; as
-// many shared-memory stages (2..4) as fit the per-CTA budget (two CTAs per SM
-// for 32 KB tiles, three for 16 KB and smaller).
+// many tile stages S (2..4, with S + 1 operand buffers) as fit the per-CTA
+// budget (two CTAs per SM for 32 KB tiles, three for 16 KB and smaller).
 template <class ST, int N, int LMAX, int CW, int UNR_>
 struct BulkTune {
   using L = RowLayout<ST, N>;
@@ -36,11 +36,12 @@ struct BulkTune {
   static constexpr int UNR = cmax(1, cmin(UNR_, cmax(1, 64 / (CW * L::RPW))));
   static constexpr int ROWS = WARPS * L::RPW * UNR;
   static constexpr int PER_STAGE = ROWS * N * (int)sizeof(ST);
-  static constexpr int FIXED = 2 * LMAX * (2 * N + 4 * ROWS) * 4;  // two vector buffers
-  static constexpr int BUDGET = (PER_STAGE > 16 * 1024 ? 110 : 72) * 1024;
-  static constexpr int S = (4 * PER_STAGE + FIXED <= BUDGET)   ? 4
-                           : (3 * PER_STAGE + FIXED <= BUDGET) ? 3
-                                                               : 2;
+  static constexpr int PER_VEC = LMAX * (2 * N + 4 * ROWS) * 4;
+  static constexpr int BUDGET = (PER_STAGE > 16 * 1024 ? 110 : 76) * 1024;
+  static constexpr int S = (4 * PER_STAGE + 5 * PER_VEC <= BUDGET)   ? 4
+                           : (3 * PER_STAGE + 4 * PER_VEC <= BUDGET) ? 3
+                                                                     : 2;
+  static constexpr int SV = S + 1;
 };
 
 template <class ST, class IT, int N, bool VARLEN, int CW, int UNR_>
@@ -48,8 +49,8 @@ cudaError_t launch_bulk_cfg(KParams p, const OneTokenArgs& oa, const VarlenArgs&
                             int64_t nitems, cudaStream_t stream) {
   constexpr int LMAX = VARLEN ? Tune<ST, N>::LMAX : 1;
   using BT = BulkTune<ST, N, LMAX, CW, UNR_>;
-  using Cfg = BulkConfig<ST, IT, N, BT::WARPS, BT::UNR, BT::S, LMAX>;
-  auto kern = ssu_bulk_kernel<ST, IT, N, BT::WARPS, BT::UNR, BT::S, LMAX, VARLEN>;
+  using Cfg = BulkConfig<ST, IT, N, BT::WARPS, BT::UNR, BT::S, BT::SV, LMAX>;
+  auto kern = ssu_bulk_kernel<ST, IT, N, BT::WARPS, BT::UNR, BT::S, BT::SV, LMAX, VARLEN>;
   p.tiles = (p.P + Cfg::ROWS - 1) / Cfg::ROWS;
   const int64_t items = nitems * (int64_t)p.H * p.tiles;
   if (items <= 0) return cudaSuccess;
@@ -74,13 +75,59 @@ cudaError_t launch_bulk_cfg(KParams p, const OneTokenArgs& oa, const VarlenArgs&
 // (16 KB, four stages, three CTAs per SM) when it is written back, in 64-row
 // tiles when it is only read (half the bytes per unit of compute); 16-bit
 // state in 64-row tiles.
+// The consumer-staged variant: two operand buffers (one per alternate item)
+// instead of a ring, the same stage budget rule.
+template <class ST, int N, int LMAX, int CW, int UNR_>
+struct BulkCsTune {
+  using L = RowLayout<ST, N>;
+  static constexpr int WARPS = CW;
+  static constexpr int UNR = cmax(1, cmin(UNR_, cmax(1, 64 / (CW * L::RPW))));
+  static constexpr int ROWS = WARPS * L::RPW * UNR;
+  static constexpr int PER_STAGE = ROWS * N * (int)sizeof(ST);
+  static constexpr int FIXED = 2 * LMAX * (2 * N + 4 * ROWS) * 4;
+  static constexpr int BUDGET = (PER_STAGE > 16 * 1024 ? 110 : 72) * 1024;
+  static constexpr int S = (4 * PER_STAGE + FIXED <= BUDGET)   ? 4
+                           : (3 * PER_STAGE + FIXED <= BUDGET) ? 3
+                                                               : 2;
+};
+
+template <class ST, class IT, int N, bool VARLEN, int CW, int UNR_>
+cudaError_t launch_bulk_cs_cfg(KParams p, const OneTokenArgs& oa, const VarlenArgs& va,
+                               int64_t nitems, cudaStream_t stream) {
+  constexpr int LMAX = VARLEN ? Tune<ST, N>::LMAX : 1;
+  using BT = BulkCsTune<ST, N, LMAX, CW, UNR_>;
+  using Cfg = BulkCsConfig<ST, IT, N, BT::WARPS, BT::UNR, BT::S, LMAX>;
+  auto kern = ssu_bulk_cs_kernel<ST, IT, N, BT::WARPS, BT::UNR, BT::S, LMAX, VARLEN>;
+  p.tiles = (p.P + Cfg::ROWS - 1) / Cfg::ROWS;
+  const int64_t items = nitems * (int64_t)p.H * p.tiles;
+  if (items <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Cfg::THREADS, Cfg::SMEM);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int64_t grid = std::min<int64_t>(items, (int64_t)sm_count() * per_sm);
+  unsigned* err = device_error_word();
+  if (!err) return cudaErrorInvalidSymbol;
+  kern<<<(unsigned)grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p, oa, va, items, err);
+  return cudaGetLastError();
+}
+
+// Which bulk pipeline and tile (measured): fp32 state that is written back
+// streams best with producer-staged operands in 32-row tiles; 16-bit state
+// and calls that write no state (more operand work per byte moved) with
+// consumer-staged operands in 64-row tiles.
 template <class ST, class IT, int N, bool VARLEN>
 cudaError_t launch_bulk(KParams p, const OneTokenArgs& oa, const VarlenArgs& va, int64_t nitems,
                         cudaStream_t stream) {
   if constexpr (sizeof(ST) == 4) {
     if (!p.disable) return launch_bulk_cfg<ST, IT, N, VARLEN, 4, 2>(p, oa, va, nitems, stream);
   }
-  return launch_bulk_cfg<ST, IT, N, VARLEN, 4, 4>(p, oa, va, nitems, stream);
+  return launch_bulk_cs_cfg<ST, IT, N, VARLEN, 4, 4>(p, oa, va, nitems, stream);
 }
 
 template <class ST, class IT, int N>
