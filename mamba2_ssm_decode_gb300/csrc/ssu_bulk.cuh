@@ -72,11 +72,27 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// descheduled until it completes or about `hint_ns` pass, instead of spinning
+// (spinning warps take issue slots from the warps that compute).
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 100000u;  // 0.1 ms per try; the phase wakes it sooner
+
 // Wait for the phase with `parity` to complete; false after `limit_ns`.
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_test(bar, parity)) {
+  while (!mbar_test_sleep(bar, parity, kSuspendHintNs)) {
     if (global_ns() - t0 > limit_ns) return false;
   }
   return true;

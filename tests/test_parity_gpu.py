@@ -51,7 +51,7 @@ def test_one_token_dtypes_and_dstate(oracle_mod, sdt, iodt, N, algo):
 @pytest.mark.parametrize("variant", ["no_z", "no_D_bias", "dt_per_dim", "dt_h1", "no_softplus",
                                      "dst_table", "in_range_pad", "out_f32", "int64",
                                      "identity", "disable", "P_ragged", "tied_A",
-                                     "per_channel", "per_channel_view"])
+                                     "per_channel", "per_channel_view", "bc_unaligned"])
 def test_one_token_variants(oracle_mod, variant, algo):
     kw = dict(batch=9, heads=4, headdim=64, dstate=128, groups=2, slots=24,
               state_dtype=torch.float32, pad_frac=0.2, seed=7, device=DEV)
@@ -100,7 +100,20 @@ def test_one_token_variants(oracle_mod, variant, algo):
         if variant == "per_channel_view":   # [H, dim, dstate] with zero dstate stride
             case.A = case.A[:, :, None].expand(4, 64, 128)
             case.dt_bias = case.dt_bias[:, :, None].expand(4, 64, 128)
+    if variant == "bc_unaligned":
+        unaligned_bc(case)
     P.parity(oracle_mod, case, out_dtype=out_dtype, label=variant, algorithm=algo)
+
+
+def unaligned_bc(case):
+    """Move B and C into one buffer at odd element offsets (rows not 16-byte aligned)."""
+    R, G, N = case.B.shape
+    big = torch.zeros(R, 2 * G * N + 3, dtype=case.B.dtype, device=case.B.device)
+    Bv = big[:, 1:1 + G * N].view(R, G, N)
+    Cv = big[:, 2 + G * N:2 + 2 * G * N].view(R, G, N)
+    Bv.copy_(case.B)
+    Cv.copy_(case.C)
+    case.B, case.C = Bv, Cv
 
 
 def test_one_token_strided_operands_bit_exact():
@@ -143,7 +156,7 @@ def test_varlen_dtypes(oracle_mod, sdt, N, algo):
 @pytest.mark.parametrize("variant", ["empty_seqs", "no_counts", "flat_tables", "dense",
                                      "same_table", "int64", "disable", "no_dst_no_src",
                                      "count_out_of_table", "long_chain", "out_f32",
-                                     "dt_per_dim", "f16_io", "per_channel"])
+                                     "dt_per_dim", "f16_io", "per_channel", "bc_unaligned"])
 def test_varlen_variants(oracle_mod, variant, algo):
     kw = dict(nseqs=7, max_len=4, heads=4, headdim=64, dstate=128, groups=2, slots=80,
               state_dtype=torch.float32, pad_frac=0.15, seed=23, device=DEV)
@@ -190,6 +203,8 @@ def test_varlen_variants(oracle_mod, variant, algo):
         case.num_accepted_tokens = na
     if variant == "out_f32":
         out_dtype = torch.float32
+    if variant == "bc_unaligned":
+        unaligned_bc(case)
     if variant == "per_channel":
         g = torch.Generator(device=DEV).manual_seed(6)
         case.A = -torch.exp(torch.rand(4, 64, generator=g, device=DEV) * 2.7)
