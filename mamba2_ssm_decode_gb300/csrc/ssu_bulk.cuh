@@ -128,10 +128,8 @@ template <int ROWS>
 __device__ __forceinline__ Item resolve_one_token(const KParams& p, const OneTokenArgs& a,
                                                   int64_t idx) {
   Item it;
-  const int tile = (int)(idx % p.tiles);
-  const int64_t rest = idx / p.tiles;
-  it.h = (int)(rest % p.H);
-  it.seq = rest / p.H;
+  int tile;
+  split_index(p, (uint32_t)idx, &it.seq, &it.h, &tile);
   it.p0 = tile * ROWS;
   it.r0 = it.seq;
   it.len = 1;
@@ -145,10 +143,8 @@ template <int ROWS>
 __device__ __forceinline__ Item resolve_varlen(const KParams& p, const VarlenArgs& a,
                                                int64_t idx) {
   Item it;
-  const int tile = (int)(idx % p.tiles);
-  const int64_t rest = idx / p.tiles;
-  it.h = (int)(rest % p.H);
-  it.seq = rest / p.H;
+  int tile;
+  split_index(p, (uint32_t)idx, &it.seq, &it.h, &tile);
   it.p0 = tile * ROWS;
   int64_t begin, end;
   if (a.cu) {
@@ -184,7 +180,7 @@ __device__ __forceinline__ Item resolve_item(const KParams& p, const OneTokenArg
 template <class ST, class IT, int N, int ROWS, int LMAX>
 __device__ __forceinline__ void stage_vectors(Stage<N, ROWS, LMAX>& s, const KParams& p,
                                               const Item& it, int t0, int n, int tid, int nthr) {
-  const int g = it.h / p.hr;
+  const int g = (int)p.fd_hr.div((uint32_t)it.h);
   const IT* Bp = static_cast<const IT*>(p.B);
   const IT* Cp = static_cast<const IT*>(p.C);
   for (int i = tid; i < n * N; i += nthr) {
@@ -261,7 +257,7 @@ struct VecPrefetch {
   // Issue the loads of steps [0, n) of item `it` (rows r0 ..).
   __device__ __forceinline__ void issue(const KParams& p, const Item& it, int n_, int tid) {
     n = n_;
-    const int g = it.h / p.hr;
+    const int g = (int)p.fd_hr.div((uint32_t)it.h);
     const IT* Bp = static_cast<const IT*>(p.B);
     const IT* Cp = static_cast<const IT*>(p.C);
 #pragma unroll
@@ -538,7 +534,7 @@ __global__ void __launch_bounds__(WARPS * 32 + 32,
         it.h = h;
         it.p0 = p0;
         it.r0 = r0;
-        it.seq = idx / p.tiles / p.H;
+        it.seq = p.fd_H.div(p.fd_tiles.div((uint32_t)idx));
         named_sync(1, Cfg::CONSUMERS);
         stage_vectors<ST, IT, N, ROWS, LMAX>(stg, p, it, t0, n, threadIdx.x, Cfg::CONSUMERS);
         named_sync(1, Cfg::CONSUMERS);
@@ -681,10 +677,8 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
   // for the packed route `cu0` / `cu1` are the sequence's cu_seqlens entries
   auto position = [&](int64_t idx, int64_t cu0, int64_t cu1) {
     Item it;
-    const int tile = (int)(idx % p.tiles);
-    const int64_t rest = idx / p.tiles;
-    it.h = (int)(rest % p.H);
-    it.seq = rest / p.H;
+    int tile;
+    split_index(p, (uint32_t)idx, &it.seq, &it.h, &tile);
     it.p0 = tile * ROWS;
     if constexpr (VARLEN) {
       int64_t begin = cu0, end = cu1;
@@ -702,7 +696,7 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
   };
   auto seq_bounds = [&](int64_t idx, int64_t* cu0, int64_t* cu1) {
     if constexpr (VARLEN) {
-      const int64_t seq = idx / p.tiles / p.H;
+      const int64_t seq = p.fd_H.div(p.fd_tiles.div((uint32_t)idx));
       if (va.cu) {
         *cu0 = load_int(va.cu, seq, va.meta64);
         *cu1 = load_int(va.cu, seq + 1, va.meta64);

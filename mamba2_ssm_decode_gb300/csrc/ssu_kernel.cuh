@@ -33,6 +33,25 @@
 
 namespace ssu {
 
+// Exact n / d for 0 <= n < 2^31 and 1 <= d < 2^31 by one high multiply, an
+// add and a shift (Granlund and Montgomery, "Division by invariant integers
+// using multiplication", 1994): with s = ceil(log2 d) and the 33-bit
+// multiplier 2^32 + m, m = floor(2^32 (2^s - d) / d) + 1, the quotient is
+// (hi32(n m) + n) >> s; n < 2^31 keeps the sum inside 32 bits.  Replaces
+// run-time 64-bit divisions (long software sequences) in the work-index
+// decomposition.
+struct FastDiv {
+  uint32_t m, s;
+  __host__ void init(uint32_t d) {
+    s = 0;
+    while ((1ull << s) < d) ++s;
+    m = (uint32_t)(((1ull << 32) * ((1ull << s) - d)) / d + 1);
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    return (__umulhi(n, m) + n) >> s;
+  }
+};
+
 // ---------------------------------------------------------------------------
 // kernel parameters (normalised on the host from ssu_params)
 // ---------------------------------------------------------------------------
@@ -63,7 +82,18 @@ struct KParams {
   int softplus;
   int disable;
   int64_t pad;
+  FastDiv fd_tiles, fd_H, fd_hr;  // divisions by tiles, H and heads per group
 };
+
+// (sequence, head, tile) of work index `idx` (< 2^31), tile fastest.
+__device__ __forceinline__ void split_index(const KParams& p, uint32_t idx, int64_t* seq, int* h,
+                                            int* tile) {
+  const uint32_t rest = p.fd_tiles.div(idx);
+  *tile = (int)(idx - rest * (uint32_t)p.tiles);
+  const uint32_t sq = p.fd_H.div(rest);
+  *h = (int)(rest - sq * (uint32_t)p.H);
+  *seq = sq;
+}
 
 struct TableArgs {
   const void* idx;  // nullptr = no table
@@ -412,7 +442,7 @@ __device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64
   const int warp = threadIdx.x >> 5;
   const int q = lane % L::LPR;   // chunk lane within the row
   const int rr = lane / L::LPR;  // row within the warp instruction
-  const int g = h / p.hr;
+  const int g = (int)p.fd_hr.div((uint32_t)h);
   const int64_t block_elems = (int64_t)p.P * N;
   ST* state = static_cast<ST*>(p.state);
 
@@ -487,11 +517,9 @@ __device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64
 template <class ST, class IT, int N, int WARPS, int UNR>
 __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     ssu_one_token_kernel(const KParams p, const OneTokenArgs a) {
-  int64_t bid = blockIdx.x;
-  const int tile = (int)(bid % p.tiles);
-  bid /= p.tiles;
-  const int h = (int)(bid % p.H);
-  const int64_t b = bid / p.H;
+  int64_t b;
+  int h, tile;
+  split_index(p, blockIdx.x, &b, &h, &tile);
   using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, 1>;
   const int p0 = tile * Cfg::ROWS;
 
@@ -506,11 +534,13 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
 template <class ST, class IT, int N, int WARPS, int UNR, int LMAX>
 __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     ssu_varlen_kernel(const KParams p, const VarlenArgs a) {
-  int64_t bid = blockIdx.x;
-  const int tile = (int)(bid % p.tiles);
-  bid /= p.tiles;
-  const int h = (int)(bid % p.H);
-  const int64_t s = bid / p.H;
+  // Plain divisions (once per CTA): at this kernel's 128-register cap the
+  // fast-division form made the register allocation spill more, and measured
+  // slower.
+  const int tile = (int)(blockIdx.x % p.tiles);
+  const int64_t rest = blockIdx.x / p.tiles;
+  const int h = (int)(rest % p.H);
+  const int64_t s = rest / p.H;
   using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
   const int p0 = tile * Cfg::ROWS;
 

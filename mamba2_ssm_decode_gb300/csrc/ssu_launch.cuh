@@ -11,6 +11,12 @@ namespace ssu {
 unsigned* device_error_word();  // this device's error word (device address)
 int sm_count();                 // SMs of the current device
 
+inline void set_divisors(KParams& p) {
+  p.fd_tiles.init((uint32_t)p.tiles);
+  p.fd_H.init((uint32_t)p.H);
+  p.fd_hr.init((uint32_t)p.hr);
+}
+
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
@@ -52,8 +58,10 @@ cudaError_t launch_bulk_cfg(KParams p, const OneTokenArgs& oa, const VarlenArgs&
   using Cfg = BulkConfig<ST, IT, N, BT::WARPS, BT::UNR, BT::S, BT::SV, LMAX>;
   auto kern = ssu_bulk_kernel<ST, IT, N, BT::WARPS, BT::UNR, BT::S, BT::SV, LMAX, VARLEN>;
   p.tiles = (p.P + Cfg::ROWS - 1) / Cfg::ROWS;
+  set_divisors(p);
   const int64_t items = nitems * (int64_t)p.H * p.tiles;
   if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
   // all of the unified L1 / shared array as shared memory: several CTAs per SM
@@ -99,8 +107,10 @@ cudaError_t launch_bulk_cs_cfg(KParams p, const OneTokenArgs& oa, const VarlenAr
   using Cfg = BulkCsConfig<ST, IT, N, BT::WARPS, BT::UNR, BT::S, LMAX>;
   auto kern = ssu_bulk_cs_kernel<ST, IT, N, BT::WARPS, BT::UNR, BT::S, LMAX, VARLEN>;
   p.tiles = (p.P + Cfg::ROWS - 1) / Cfg::ROWS;
+  set_divisors(p);
   const int64_t items = nitems * (int64_t)p.H * p.tiles;
   if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -145,6 +155,7 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
                   : launch_bulk<ST, IT, N, false>(p, o0, v0, nitems, stream);
   }
   p.tiles = (p.P + Cfg::ROWS - 1) / Cfg::ROWS;
+  set_divisors(p);
   const int64_t grid = nitems * (int64_t)p.H * p.tiles;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
