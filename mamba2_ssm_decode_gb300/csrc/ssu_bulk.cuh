@@ -9,17 +9,18 @@
 // 16-32 KB per CTA stay in flight continuously while the consumer warps work.
 //
 // Work item = (sequence, head, row tile of ROWS headdim rows); a CTA walks the
-// items blockIdx.x, blockIdx.x + gridDim.x, ...  For item k on stage s = k % S:
-//   producer (one thread): resolve the item's slots (one item ahead, so the
-//     index loads are in flight while it waits), wait empty[s] (the consumers
-//     released item k - S), publish the slots in the stage's record, arm
-//     full[s] with the tile's byte count and issue one bulk copy of its
-//     contiguous rows (or just arrive for a pad / invalid read slot);
-//   consumer warps: stage the item's per-step vectors (B, C, dA, dt' x, D x,
-//     silu z) into one of two shared buffers with one round of loads while the
-//     copy lands, wait full[s], read their chunks of the tile into fp32
-//     registers, release empty[s] at once, then run the steps exactly as the
-//     register kernel does (same lane layout, same arithmetic, same stores).
+// items blockIdx.x, blockIdx.x + gridDim.x, ...  For item k on stage s = k % S
+// one producer thread resolves the item's slots (one item ahead, so the index
+// loads are in flight while it waits), waits until stage s is free, publishes
+// the slots, arms full[s] with the tile's byte count and issues one bulk copy
+// of the tile's contiguous rows (or just arrives, for a pad / invalid read
+// slot).  The consumer warps wait full[s], read their chunks of the tile into
+// fp32 registers, release the stage at once, then run the steps exactly as the
+// register kernel does (same lane layout, same arithmetic, same stores).
+// Two kernels differ in who stages the item's per-step operands (B, C, dA,
+// dt' x, D x, silu z): in ssu_bulk_kernel the producer warp converts them into
+// a ring of operand buffers one item ahead; in ssu_bulk_cs_kernel the consumer
+// warps load them with one round of loads while the copy lands.
 // Every wait is bounded (2 s of global time); a wait that runs out records an
 // error code in *err and the CTA leaves after its own copies have landed.
 #pragma once
