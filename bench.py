@@ -426,7 +426,8 @@ EXTRAS = ["hybrid-grouped-decode", "mtp-varlen",
           "sweep-mtp-float32-b1024", "sweep-mtp-bfloat16-b1024",
           "sweep-single-float32-b4096", "sweep-single-bfloat16-b4096",
           "sweep-mtp-float32-b4096", "sweep-mtp-bfloat16-b4096",
-          "sweep-single-float32-b1024-nowrite", "sweep-single-bfloat16-b1024-nowrite"]
+          "sweep-single-float32-b1024-nowrite", "sweep-single-bfloat16-b1024-nowrite",
+          "sweep-mtp-float32-b1024-nowrite", "sweep-mtp-bfloat16-b1024-nowrite"]
 
 
 def dist_setup(n_gpus):

@@ -64,14 +64,22 @@ typedef enum ssu_status {
  * Kernel selection (the pages' SSU entry points carry an `algorithm` choice
  * too: "ssu_dispatch" forwards MambaConfig.ssu_algorithm, "mate.mamba"
  * accepts auto/simple/vertical/horizontal and runs one kernel for all).
- *   SSU_ALGO_AUTO    the library's choice: BULK for ssu_update, DIRECT for
- *                    ssu_update_varlen (the faster of the two on each)
+ *   SSU_ALGO_AUTO    the library's choice, the faster as measured: BULK for
+ *                    ssu_update (DIRECT for 16-bit state with
+ *                    disable_state_update), DIRECT for ssu_update_varlen
  *   SSU_ALGO_DIRECT  one CTA per (sequence, head, 64-row tile); each thread
- *                    loads its state chunks straight into registers
+ *                    loads its state chunks straight into registers.  With
+ *                    disable_state_update: one CTA per (sequence, run of
+ *                    heads of one group, row tile), state tiles copied
+ *                    asynchronously into shared memory, and the steps of a
+ *                    chain in closed form (no state is stored, so y_t needs
+ *                    only C_t . h, C_t . B_s and products of dA)
  *   SSU_ALGO_BULK    persistent CTAs; a producer warp streams each tile into a
  *                    ring of shared-memory stages with one bulk asynchronous
  *                    copy while consumer warps compute
- * Both compute the same arithmetic in the same order (bit-identical results).
+ * For calls that write state both compute the same arithmetic in the same
+ * order (bit-identical results); for calls that write none the closed form
+ * rounds differently (within the same tolerances).
  */
 typedef enum ssu_algorithm {
   SSU_ALGO_AUTO = 0,

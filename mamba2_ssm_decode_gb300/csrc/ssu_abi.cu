@@ -150,6 +150,13 @@ ssu_status check_params(const ssu_params* p, ssu::KParams* k) {
   k->C = p->C;
   k->C_rs = p->C_row_stride;
   k->C_gs = p->C_group_stride;
+  {
+    // 16-bit B / C: 8 elements per 16 bytes
+    auto a16 = [](const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; };
+    k->bc_vec16 = a16(p->B) && a16(p->C) && p->B_row_stride % 8 == 0 &&
+                  p->B_group_stride % 8 == 0 && p->C_row_stride % 8 == 0 &&
+                  p->C_group_stride % 8 == 0;
+  }
   k->A = p->A;
   k->A_s = p->A_stride;
   k->A_ds = p->A_dim_stride;

@@ -81,6 +81,7 @@ struct KParams {
   int64_t bias_s, bias_ds;
   int softplus;
   int disable;
+  int bc_vec16;  // B and C rows start on 16-byte boundaries (pointer and strides)
   int64_t pad;
   FastDiv fd_tiles, fd_H, fd_hr;  // divisions by tiles, H and heads per group
 };
@@ -511,6 +512,32 @@ __device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64
       }
     }
   }
+}
+
+// Slots and rows of packed sequence s; false for an empty sequence.
+__device__ __forceinline__ bool varlen_item(const KParams& p, const VarlenArgs& a, int64_t s,
+                                            int64_t* r0, int* len, int64_t* src, bool* read_ok) {
+  int64_t begin, end;
+  if (a.cu) {
+    begin = load_int(a.cu, s, a.meta64);
+    end = load_int(a.cu, s + 1, a.meta64);
+  } else {
+    begin = s * a.dense_steps;
+    end = begin + a.dense_steps;
+  }
+  if (begin < 0) begin = 0;
+  if (end > a.rows) end = a.rows;
+  if (end <= begin) return false;
+  *r0 = begin;
+  *len = (int)(end - begin);
+  *src = s;
+  bool ok = true;
+  if (a.src.idx) {
+    const int64_t col = a.na ? load_int(a.na, s, a.meta64) - 1 : 0;
+    ok = table_entry(a.src, s, col, a.idx64, src);
+  }
+  *read_ok = ok && slot_ok(*src, p.pad, p.slots);
+  return true;
 }
 
 // One-token decode: blockIdx -> (sequence b, head, row tile).

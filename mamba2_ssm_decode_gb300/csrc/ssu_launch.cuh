@@ -4,6 +4,7 @@
 #include <algorithm>
 
 #include "ssu_bulk.cuh"
+#include "ssu_nowrite.cuh"
 
 namespace ssu {
 
@@ -29,6 +30,16 @@ struct Tune {
   static constexpr int WARPS = 4;
   static constexpr int UNR = cmax(1, cmin(64 / (WARPS * L::RPW), cmax(1, 64 / L::EPL)));
   static constexpr int LMAX = 4;
+};
+
+// No-write kernel: state tiles of at most 16 KB, two per CTA.
+template <class ST, int N>
+struct NoWriteTune {
+  using L = RowLayout<ST, N>;
+  static constexpr int WARPS = 4;
+  static constexpr int UNR = cmax(
+      1, cmin(Tune<ST, N>::UNR, 16384 / (WARPS * L::RPW * N * (int)sizeof(ST))));
+  static constexpr int ROWS = WARPS * L::RPW * UNR;
 };
 
 // Bulk-copy pipeline shape: CW consumer warps, each thread owning UNR state
@@ -145,19 +156,50 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
                          int64_t nitems, cudaStream_t stream, int algorithm) {
   using T = Tune<ST, N>;
   using Cfg = SSUConfig<ST, IT, N, T::WARPS, T::UNR, T::LMAX>;
-  // auto: the bulk-copy pipeline for one-token calls, the register kernel for
-  // multi-token chains (the faster of the two on each, as measured)
-  const bool bulk = algorithm == 2 /* SSU_ALGO_BULK */ || (algorithm == 0 && !varlen);
+  // auto (the fastest as measured): the bulk-copy pipeline for one-token calls,
+  // except 16-bit state with no state written (the no-write kernel); the
+  // register kernel for multi-token chains, the no-write kernel for those
+  // that write no state
+  const bool auto_bulk = !varlen && (!p.disable || sizeof(ST) == 4);
+  const bool bulk = algorithm == 2 /* SSU_ALGO_BULK */ || (algorithm == 0 && auto_bulk);
   if (bulk) {
     const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
     const VarlenArgs v0 = va ? *va : VarlenArgs{};
     return varlen ? launch_bulk<ST, IT, N, true>(p, o0, v0, nitems, stream)
                   : launch_bulk<ST, IT, N, false>(p, o0, v0, nitems, stream);
   }
+  if (nitems <= 0) return cudaSuccess;
+  if (p.disable) {
+    // no-write kernel: grid (row tiles, runs of kh heads of one group,
+    // sequences); kh is the largest of 8, 4, 2, 1 dividing the heads per
+    // group, and y / z extents are limited to 65535, so longer batches go in
+    // several launches of up to 65535 sequences
+    using NT = NoWriteTune<ST, N>;
+    const int kh = p.hr % 8 == 0 ? 8 : p.hr % 4 == 0 ? 4 : p.hr % 2 == 0 ? 2 : 1;
+    p.tiles = (p.P + NT::ROWS - 1) / NT::ROWS;
+    set_divisors(p);
+    if (p.H / kh > 65535) return cudaErrorInvalidConfiguration;
+    auto kern = varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
+                       : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
+    // several CTAs of up to 45 KB static shared memory per SM: ask for the
+    // largest shared-memory carveout
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
+    const VarlenArgs v0 = va ? *va : VarlenArgs{};
+    constexpr int64_t kZ = 65535;
+    for (int64_t s0 = 0; s0 < nitems; s0 += kZ) {
+      const dim3 grid((unsigned)p.tiles, (unsigned)(p.H / kh), (unsigned)std::min(kZ, nitems - s0));
+      kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, s0, kh);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   p.tiles = (p.P + Cfg::ROWS - 1) / Cfg::ROWS;
   set_divisors(p);
   const int64_t grid = nitems * (int64_t)p.H * p.tiles;
-  if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (varlen) {
     ssu_varlen_kernel<ST, IT, N, T::WARPS, T::UNR, T::LMAX>

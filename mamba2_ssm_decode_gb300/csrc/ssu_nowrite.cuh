@@ -1,0 +1,541 @@
+// ssu_nowrite.cuh -- the SSU for calls that write no state
+// (disable_state_update).
+//
+// With no state to store, the steps of a staged chunk have a closed form.
+// Unrolling h_t = dA_t h_{t-1} + dtx_t B_t from the chunk's initial state h:
+//   C_t . h_t = P_t (C_t . h) + sum_{s <= t} E_{s,t} (C_t . B_s),
+//   P_t = dA_0 dA_1 ... dA_t,   E_{s,t} = dtx_s dA_{s+1} ... dA_t.
+// A state element then costs one FMA per step (the dot products C_t . h)
+// instead of three, the products G[t][s] = C_t . B_s are formed once per
+// CTA, and the state never has to sit in registers: it lands in shared
+// memory by cp.async.  A CTA takes several heads of one group for one
+// sequence, so the slot lookup, the B / C staging and G are done once for
+// all of them, and the next head's tile (contiguous in the slot) is in
+// flight while the current one is computed.
+#pragma once
+
+#include "ssu_kernel.cuh"
+
+namespace ssu {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem), "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// wait until at most `pending` of this thread's newest copy groups are in flight
+template <int pending>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(pending) : "memory");
+}
+
+// Lane q's values of its chunk c of a staged row (B / C layout of bc_slot), as pairs.
+template <class ST, int N>
+__device__ __forceinline__ void lane_chunk(const float* row, int q, int c, float2* v) {
+  using L = RowLayout<ST, N>;
+  constexpr int H4 = L::VEC / 4;
+#pragma unroll
+  for (int h = 0; h < H4; ++h) {
+    const float4 f = *reinterpret_cast<const float4*>(&row[((c * H4 + h) * L::LPR + q) * 4]);
+    v[2 * h] = make_float2(f.x, f.y);
+    v[2 * h + 1] = make_float2(f.z, f.w);
+  }
+}
+
+template <int N, int LMAX>
+struct __align__(16) StepsBC {
+  float B[LMAX][N];
+  float C[LMAX][N];
+};
+
+template <int ROWS, int LMAX>
+struct __align__(16) HeadRows {
+  float dA[LMAX][ROWS];
+  float dtx[LMAX][ROWS];   // dt' * x
+  float Dx[LMAX][ROWS];    // D * x
+  float gate[LMAX][ROWS];  // silu(z), or 1
+};
+
+// B and C rows of group g for steps [t0, t0 + n), in the bc_slot layout:
+// 16-byte loads of 8 elements where the rows allow them (bc_slot keeps
+// every aligned run of 4 columns contiguous), element loads otherwise.
+template <class ST, class IT, int N, int LMAX, int THREADS, class BC>
+__device__ __forceinline__ void stage_bc(BC& s, const KParams& p, int64_t r0, int t0, int n,
+                                         int g) {
+  const IT* Bp = static_cast<const IT*>(p.B);
+  const IT* Cp = static_cast<const IT*>(p.C);
+  if (p.bc_vec16) {
+    constexpr int V8 = N / 8;  // 16-byte pieces per row
+    for (int i = threadIdx.x; i < 2 * n * V8; i += THREADS) {
+      const bool isC = i >= n * V8;
+      const int ii = isC ? i - n * V8 : i;
+      const int tt = ii / V8, k0 = (ii - tt * V8) * 8;
+      const int64_t r = r0 + t0 + tt;
+      const IT* src = isC ? Cp + r * p.C_rs + (int64_t)g * p.C_gs + k0
+                          : Bp + r * p.B_rs + (int64_t)g * p.B_gs + k0;
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
+      const IT* e = reinterpret_cast<const IT*>(&w);
+      float* row = isC ? s.C[tt] : s.B[tt];
+      *reinterpret_cast<float4*>(&row[bc_slot<ST, N>(k0)]) =
+          make_float4(io_to_float<IT>(e[0]), io_to_float<IT>(e[1]), io_to_float<IT>(e[2]),
+                      io_to_float<IT>(e[3]));
+      *reinterpret_cast<float4*>(&row[bc_slot<ST, N>(k0 + 4)]) =
+          make_float4(io_to_float<IT>(e[4]), io_to_float<IT>(e[5]), io_to_float<IT>(e[6]),
+                      io_to_float<IT>(e[7]));
+    }
+    return;
+  }
+  for (int i = threadIdx.x; i < n * N; i += THREADS) {
+    const int tt = i / N, k = i - tt * N;
+    const int64_t r = r0 + t0 + tt;
+    s.B[tt][bc_slot<ST, N>(k)] = io_to_float<IT>(Bp[r * p.B_rs + (int64_t)g * p.B_gs + k]);
+    s.C[tt][bc_slot<ST, N>(k)] = io_to_float<IT>(Cp[r * p.C_rs + (int64_t)g * p.C_gs + k]);
+  }
+}
+
+// dt' = softplus(dt + dt_bias) and dA = exp(A dt') of heads h0 .. h0 + kh - 1
+// for steps [0, n), when dt, A and dt_bias are per head (ignored otherwise).
+template <int KMAX, int LMAX>
+struct HeadSteps {
+  float dt[KMAX][LMAX];
+  float dA[KMAX][LMAX];
+};
+
+// dt, A and dt_bias all per head: dt' and dA do not depend on the row
+__device__ __forceinline__ bool per_head_dt(const KParams& p) {
+  return p.dt_ds == 0 && p.A_ds == 0 && (!p.dt_bias || p.bias_ds == 0);
+}
+
+template <int KMAX, int LMAX>
+__device__ __forceinline__ void stage_head_steps(HeadSteps<KMAX, LMAX>& s, const KParams& p,
+                                                 int64_t r0, int n, int h0, int kh) {
+  const int i = threadIdx.x;
+  if (i >= kh * LMAX) return;
+  const int k = i / LMAX, t = i % LMAX;
+  if (t >= n) return;
+  const int h = h0 + k;
+  float d = p.dt[(r0 + t) * p.dt_rs + (int64_t)h * p.dt_hs] +
+            (p.dt_bias ? p.dt_bias[(int64_t)h * p.bias_s] : 0.0f);
+  if (p.softplus) d = softplus_f(d);
+  s.dt[k][t] = d;
+  s.dA[k][t] = expf(p.A[(int64_t)h * p.A_s] * d);
+}
+
+// The per-row scalars of one head in two halves, so that the loads of the
+// next head are in flight while the current head computes: load() issues
+// this thread's global loads into registers, finish() evaluates and stores
+// them.  Thread i keeps step i % LMAX of rows i / LMAX + m THREADS / LMAX;
+// their x / z offsets within a head are fixed, so they are formed once.
+template <class IT, int ROWS, int LMAX, int THREADS>
+struct RowPrefetch {
+  static_assert(THREADS % LMAX == 0, "a thread keeps one step");
+  static constexpr int NP = (ROWS * LMAX + THREADS - 1) / THREADS;  // rows per thread
+  float x[NP], z[NP], D[NP], dt[NP], A[NP], bias[NP];
+  int64_t xo[NP], zo[NP];
+  int prow[NP];
+  int t;
+  int64_t r;  // packed row of step t
+
+  __device__ __forceinline__ void init(const KParams& p, int64_t r0, int n, int p0) {
+    t = threadIdx.x % LMAX;
+    r = r0 + t;
+#pragma unroll
+    for (int m = 0; m < NP; ++m) {
+      const int j = threadIdx.x / LMAX + m * (THREADS / LMAX);
+      prow[m] = (t < n && j < ROWS && p0 + j < p.P) ? p0 + j : -1;
+      xo[m] = (r0 + t) * p.x_rs + prow[m];
+      zo[m] = (r0 + t) * p.z_rs + prow[m];
+    }
+  }
+
+  __device__ __forceinline__ void load(const KParams& p, int h, bool tied) {
+    const IT* xp = static_cast<const IT*>(p.x);
+    const IT* zp = static_cast<const IT*>(p.z);
+#pragma unroll
+    for (int m = 0; m < NP; ++m) {
+      x[m] = z[m] = D[m] = dt[m] = A[m] = bias[m] = 0.0f;
+      if (prow[m] >= 0) {
+        x[m] = io_to_float<IT>(xp[xo[m] + (int64_t)h * p.x_hs]);
+        if (zp) z[m] = io_to_float<IT>(zp[zo[m] + (int64_t)h * p.z_hs]);
+        if (p.D) D[m] = p.D[(int64_t)h * p.D_s + (int64_t)prow[m] * p.D_ds];
+        if (!tied) {
+          dt[m] = p.dt[r * p.dt_rs + (int64_t)h * p.dt_hs + (int64_t)prow[m] * p.dt_ds];
+          A[m] = p.A[(int64_t)h * p.A_s + (int64_t)prow[m] * p.A_ds];
+          if (p.dt_bias)
+            bias[m] = p.dt_bias[(int64_t)h * p.bias_s + (int64_t)prow[m] * p.bias_ds];
+        }
+      }
+    }
+  }
+
+  // hdt / hdA: this head's per-head dt' and dA by step (used when tied)
+  template <class HR>
+  __device__ __forceinline__ void finish(HR& s, const KParams& p, int n, int p0, bool tied,
+                                         const float* hdt, const float* hdA) const {
+    if (t >= n) return;
+#pragma unroll
+    for (int m = 0; m < NP; ++m) {
+      const int j = threadIdx.x / LMAX + m * (THREADS / LMAX);
+      if (j >= ROWS) break;
+      float dAv = 1.0f, dtx = 0.0f, Dx = 0.0f, gate = 1.0f;
+      if (prow[m] >= 0) {
+        float dtv;
+        if (tied) {
+          dtv = hdt[t];
+          dAv = hdA[t];
+        } else {
+          dtv = dt[m] + bias[m];
+          if (p.softplus) dtv = softplus_f(dtv);
+          dAv = expf(A[m] * dtv);
+        }
+        dtx = dtv * x[m];
+        Dx = D[m] * x[m];
+        if (p.z) gate = __fdividef(z[m], 1.0f + __expf(-z[m]));
+      }
+      s.dA[t][j] = dAv;
+      s.dtx[t][j] = dtx;
+      s.Dx[t][j] = Dx;
+      s.gate[t][j] = gate;
+    }
+  }
+};
+
+// G[t][s] = C_t . B_s for s <= t < n; pair k goes to warp k % WARPS.
+template <int N, int LMAX, int WARPS, class BC>
+__device__ __forceinline__ void stage_G(const BC& bc, float (&G)[LMAX][LMAX], int n, int warp,
+                                        int lane) {
+  int k = 0;
+#pragma unroll
+  for (int t = 0; t < LMAX; ++t) {
+#pragma unroll
+    for (int s = 0; s <= t; ++s, ++k) {
+      if (t < n && (k % WARPS) == warp) {
+        float v = 0.0f;
+        for (int i = lane; i < N; i += 32) v = fmaf(bc.C[t][i], bc.B[s][i], v);
+        v = warp_sum(v);
+        if (lane == 0) G[t][s] = v;
+      }
+    }
+  }
+}
+
+// y of steps t < n (rows r + t) for row j of the tile, from ct[t] = C_t . h.
+template <class IT, int LMAX, class HR>
+__device__ __forceinline__ void closed_form_y(const KParams& p, const HR& hr,
+                                              const float (&G)[LMAX][LMAX], const float* ct,
+                                              int n, int j, int h, int prow, int64_t r) {
+  float e[LMAX];
+  float P = 1.0f;
+#pragma unroll
+  for (int t = 0; t < LMAX; ++t) {
+    if (t >= n) break;
+    const float dA = hr.dA[t][j];
+    P *= dA;
+#pragma unroll
+    for (int s = 0; s < t; ++s) e[s] *= dA;
+    e[t] = hr.dtx[t][j];
+    float v = P * ct[t];
+#pragma unroll
+    for (int s = 0; s <= t; ++s) v = fmaf(e[s], G[t][s], v);
+    const float yv = (v + hr.Dx[t][j]) * hr.gate[t][j];
+    const int64_t o = (r + t) * p.o_rs + (int64_t)h * p.o_hs + prow;
+    if (p.out_f32) static_cast<float*>(p.out)[o] = yv;
+    else static_cast<IT*>(p.out)[o] = float_to_io<IT>(yv);
+  }
+}
+
+// y of step t (row r + t) for row j, from ct = C_t . h: the sum over s runs
+// from t down, so one running product gives E_{s,t} and, at the end, P_t.
+template <class IT, int LMAX, class HR>
+__device__ __forceinline__ void closed_form_y_step(const KParams& p, const HR& hr,
+                                                   const float (&G)[LMAX][LMAX], float ct, int t,
+                                                   int j, int h, int prow, int64_t r) {
+  float v = 0.0f, prod = 1.0f;
+#pragma unroll
+  for (int s = LMAX - 1; s >= 0; --s) {
+    if (s > t) continue;
+    v = fmaf(prod * hr.dtx[s][j], G[t][s], v);
+    prod *= hr.dA[s][j];
+  }
+  const float yv = (fmaf(prod, ct, v) + hr.Dx[t][j]) * hr.gate[t][j];
+  const int64_t o = (r + t) * p.o_rs + (int64_t)h * p.o_hs + prow;
+  if (p.out_f32) static_cast<float*>(p.out)[o] = yv;
+  else static_cast<IT*>(p.out)[o] = float_to_io<IT>(yv);
+}
+
+// Register form for chains longer than one staged chunk: the earlier chunks
+// run the step-by-step update (the next chunk needs their state), the last
+// one the closed form.
+template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, class StageT>
+__device__ __noinline__ void ssu_block_nowrite_chain(const KParams& p, int h, int p0, int64_t r0,
+                                                     int len, int64_t src, bool read_ok,
+                                                     StageT& stg, float (&G)[LMAX][LMAX]) {
+  using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
+  using L = typename Cfg::L;
+  constexpr int ROWS = Cfg::ROWS;
+  constexpr int THREADS = Cfg::THREADS;
+  constexpr int C2 = L::VEC / 2;                          // element pairs per chunk
+  constexpr int LEFT = UNR > L::LPR ? UNR / L::LPR : 1;  // rows a lane owns after the reduce
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int q = lane % L::LPR;
+  const int rr = lane / L::LPR;
+  const int g = (int)p.fd_hr.div((uint32_t)h);
+  const int64_t block_elems = (int64_t)p.P * N;
+  const ST* state = static_cast<const ST*>(p.state);
+
+  float2 hs[UNR][L::EPL / 2];
+  {
+    const ST* base = state + (((read_ok ? src : 0) * p.H + h) * block_elems);
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int prow = p0 + (warp * UNR + u) * L::RPW + rr;
+      const bool ok = read_ok && prow < p.P;
+#pragma unroll
+      for (int c = 0; c < L::CPL; ++c) {
+        const uint4 raw = ok ? ld_stream(base + (int64_t)prow * N + (q + c * L::LPR) * L::VEC)
+                             : make_uint4(0u, 0u, 0u, 0u);
+        Elem<ST>::unpack2(raw, &hs[u][c * L::VEC / 2]);
+      }
+    }
+  }
+  const int jbase = warp * UNR * L::RPW + rr;
+  for (int t0 = 0; t0 < len; t0 += LMAX) {
+    const int n = (len - t0) < LMAX ? (len - t0) : LMAX;
+    __syncthreads();  // the stage is free
+    stage_steps<ST, IT, N, ROWS, LMAX, THREADS>(stg, p, r0, t0, n, h, g, p0);
+    __syncthreads();
+    if (t0 + n < len) {
+#pragma unroll
+      for (int tt = 0; tt < LMAX; ++tt) {
+        if (tt >= n) break;
+        step_rows<ST, IT, N, UNR>(hs, stg, tt, q, jbase, p, h, p0, r0 + t0 + tt);
+      }
+      continue;
+    }
+    stage_G<N, LMAX, WARPS>(stg, G, n, warp, lane);
+    float ct[LEFT][LMAX];
+    int base = 0, plain = 0;
+#pragma unroll
+    for (int t = 0; t < LMAX; ++t) {
+      if (t >= n) break;
+      float2 a2[UNR];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) a2[u] = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int c = 0; c < L::CPL; ++c) {
+        float2 cv[C2];
+        lane_chunk<ST, N>(stg.C[t], q, c, cv);
+#pragma unroll
+        for (int u = 0; u < UNR; ++u)
+#pragma unroll
+          for (int i = 0; i < C2; ++i) a2[u] = __ffma2_rn(hs[u][c * C2 + i], cv[i], a2[u]);
+      }
+      float acc[UNR];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) acc[u] = a2[u].x + a2[u].y;
+      base = 0;
+      plain = 0;
+      RowScatter<UNR, L::LPR / 2>::run(acc, q, base, plain);
+#pragma unroll
+      for (int i = 0; i < LEFT; ++i) ct[i][t] = acc[i];
+    }
+    __syncthreads();  // G complete
+    if ((q & plain) == 0) {
+#pragma unroll
+      for (int i = 0; i < LEFT; ++i) {
+        const int j = jbase + (base + i) * L::RPW;
+        if (p0 + j < p.P) closed_form_y<IT, LMAX>(p, stg, G, ct[i], n, j, h, p0 + j, r0 + t0);
+      }
+    }
+  }
+}
+
+// No-write kernel, one-token and packed routes: grid (row tiles, head runs
+// of kh heads of one group, sequences seq0 + z).  Sequences longer than
+// LMAX take the register form, head by head.
+template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, bool VARLEN>
+__global__ void __launch_bounds__(WARPS * 32, 5)
+    ssu_nowrite_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t seq0,
+                       int kh) {
+  using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
+  using L = typename Cfg::L;
+  constexpr int ROWS = Cfg::ROWS;
+  using StageT = Stage<N, ROWS, LMAX>;
+  constexpr int THREADS = Cfg::THREADS;
+  constexpr int C2 = L::VEC / 2;
+  constexpr int LEFT = UNR > L::LPR ? UNR / L::LPR : 1;  // rows a lane owns after a reduce
+  constexpr bool JOINT = LMAX * UNR == L::LPR;           // one (step, row) sum per lane
+  constexpr int TILE_BYTES = ROWS * N * (int)sizeof(ST);
+  constexpr int RAW =
+      2 * TILE_BYTES > (int)sizeof(StageT) ? 2 * TILE_BYTES : (int)sizeof(StageT);
+  __shared__ __align__(128) unsigned char raw[RAW];  // two state tiles, or a chain's stage
+  __shared__ StepsBC<N, LMAX> bc;
+  __shared__ HeadRows<ROWS, LMAX> hrows[2];
+  __shared__ HeadSteps<8, LMAX> hsteps;
+  __shared__ float G[LMAX][LMAX];
+
+  const int64_t s = seq0 + blockIdx.z;
+  const int h0 = (int)blockIdx.y * kh;
+  const int p0 = (int)blockIdx.x * ROWS;
+  int64_t r0, src;
+  int len;
+  bool read_ok;
+  if constexpr (VARLEN) {
+    if (!varlen_item(p, va, s, &r0, &len, &src, &read_ok)) return;
+  } else {
+    r0 = s;
+    len = 1;
+    src = oa.sbi ? load_int(oa.sbi, s, oa.idx64) : s;
+    read_ok = slot_ok(src, p.pad, p.slots);
+  }
+  if (len > LMAX) {
+    StageT& stg = *reinterpret_cast<StageT*>(raw);
+    for (int k = 0; k < kh; ++k)
+      ssu_block_nowrite_chain<ST, IT, N, WARPS, UNR, LMAX>(p, h0 + k, p0, r0, len, src, read_ok,
+                                                           stg, G);
+    return;
+  }
+
+  // 1. state tiles of the first two heads by 16-byte async copies (zero fill
+  //    past P or without a read slot), one commit group per head
+  const int64_t block_elems = (int64_t)p.P * N;
+  const int nrows = p.P - p0 < ROWS ? p.P - p0 : ROWS;
+  const int valid = read_ok ? nrows * N * (int)sizeof(ST) / 16 : 0;
+  const char* slot_rows = reinterpret_cast<const char*>(
+      static_cast<const ST*>(p.state) + (read_ok ? src : 0) * p.H * block_elems +
+      (int64_t)p0 * N);
+  auto issue_tile = [&](int k, int buf) {
+    if (k < kh) {
+      const char* gsrc = slot_rows + (size_t)(h0 + k) * block_elems * sizeof(ST);
+      unsigned char* dst = raw + buf * TILE_BYTES;
+#pragma unroll 4
+      for (int i = threadIdx.x; i < TILE_BYTES / 16; i += THREADS) {
+        const bool v = i < valid;
+        cp_async16(dst + i * 16, v ? gsrc + (size_t)i * 16 : static_cast<const char*>(p.state),
+                   v ? 16 : 0);
+      }
+    }
+    cp_async_commit();
+  };
+  issue_tile(0, 0);
+  issue_tile(1, 1);
+
+  // 2. the steps' B / C (shared by the run's heads), the first head's rows and G
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const bool tied = per_head_dt(p);
+  RowPrefetch<IT, ROWS, LMAX, THREADS> pre;
+  pre.init(p, r0, len, p0);
+  pre.load(p, h0, tied);
+  stage_bc<ST, IT, N, LMAX, THREADS>(bc, p, r0, 0, len, (int)p.fd_hr.div((uint32_t)h0));
+  if (tied) stage_head_steps<8, LMAX>(hsteps, p, r0, len, h0, kh);
+  __syncthreads();
+  pre.finish(hrows[0], p, len, p0, tied, hsteps.dt[0], hsteps.dA[0]);
+  stage_G<N, LMAX, WARPS>(bc, G, len, warp, lane);
+
+  const int q = lane % L::LPR;
+  const int rr = lane / L::LPR;
+  const int jbase = warp * UNR * L::RPW + rr;
+  for (int k = 0; k < kh; ++k) {
+    cp_async_wait<1>();  // head k's copies (the newest group is head k + 1's)
+    __syncthreads();     // ... from every thread; hrows[k & 1] and G complete
+    const unsigned char* tile = raw + (k & 1) * TILE_BYTES;
+
+    // 3. ct[t] = C_t . h for this thread's rows: one pass over the tile
+    if (k + 1 < kh) pre.load(p, h0 + k + 1, tied);  // in flight meanwhile
+    float2 a2[LMAX][UNR];  // even / odd element partial sums
+    if constexpr (!JOINT) {
+#pragma unroll
+      for (int t = 0; t < LMAX; ++t)
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) a2[t][u] = make_float2(0.0f, 0.0f);
+    }
+#pragma unroll
+    for (int c = 0; c < L::CPL; ++c) {
+      float2 cv[LMAX][C2];  // chunk c of every step's C, read once for all rows
+#pragma unroll
+      for (int t = 0; t < LMAX; ++t)
+        if (t < len) lane_chunk<ST, N>(bc.C[t], q, c, cv[t]);
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int j = jbase + u * L::RPW;
+        float2 hv[C2];
+        Elem<ST>::unpack2(*reinterpret_cast<const uint4*>(
+                              tile + ((size_t)j * N + (q + c * L::LPR) * L::VEC) * sizeof(ST)),
+                          hv);
+#pragma unroll
+        for (int t = 0; t < LMAX; ++t) {
+          if (t >= len) break;
+#pragma unroll
+          for (int i = 0; i < C2; ++i)
+            a2[t][u] = (JOINT && c == 0 && i == 0) ? __fmul2_rn(hv[i], cv[t][i])
+                                                   : __ffma2_rn(hv[i], cv[t][i], a2[t][u]);
+        }
+      }
+    }
+    // Where the (step, row) sums number exactly the lanes of a row group, one
+    // reduce-scatter over all of them (value v = t UNR + u) leaves every lane
+    // one y to form; otherwise one reduce-scatter per step over the rows.
+    float acc[JOINT ? LMAX * UNR : 1];
+    float ct[JOINT ? 1 : LEFT][LMAX];
+    int base = 0, plain = 0;
+    if constexpr (JOINT) {
+#pragma unroll
+      for (int t = 0; t < LMAX; ++t)
+#pragma unroll
+        for (int u = 0; u < UNR; ++u)
+          acc[t * UNR + u] = t < len ? a2[t][u].x + a2[t][u].y : 0.0f;
+      RowScatter<LMAX * UNR, L::LPR / 2>::run(acc, q, base, plain);
+    } else {
+#pragma unroll
+      for (int t = 0; t < LMAX; ++t) {
+        if (t >= len) break;
+        float rs[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) rs[u] = a2[t][u].x + a2[t][u].y;
+        base = 0;
+        plain = 0;
+        RowScatter<UNR, L::LPR / 2>::run(rs, q, base, plain);
+#pragma unroll
+        for (int i = 0; i < LEFT; ++i) ct[i][t] = rs[i];
+      }
+    }
+
+    // 4. the next head's rows; then the tile buffer goes to head k + 2
+    if (k + 1 < kh)
+      pre.finish(hrows[(k + 1) & 1], p, len, p0, tied, hsteps.dt[k + 1], hsteps.dA[k + 1]);
+    __syncthreads();  // every thread is done with tile k; hrows[(k + 1) & 1] complete
+    issue_tile(k + 2, k & 1);
+
+    // 5. y of head k
+    if constexpr (JOINT) {
+      const int t = base / UNR, u = base - t * UNR;
+      const int j = jbase + u * L::RPW;
+      if (t < len && p0 + j < p.P)
+        closed_form_y_step<IT, LMAX>(p, hrows[k & 1], G, acc[0], t, j, h0 + k, p0 + j, r0);
+    } else if ((q & plain) == 0) {
+#pragma unroll
+      for (int i = 0; i < LEFT; ++i) {
+        const int j = jbase + (base + i) * L::RPW;
+        if (p0 + j < p.P)
+          closed_form_y<IT, LMAX>(p, hrows[k & 1], G, ct[i], len, j, h0 + k, p0 + j, r0);
+      }
+    }
+  }
+}
+
+}  // namespace ssu

@@ -140,6 +140,62 @@ def test_one_token_strided_operands_bit_exact():
 
 
 # ---------------------------------------------------------------------------
+# calls that write no state (disable_state_update): the register kernel takes
+# the closed form of the chain, so every lane layout is checked here too
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("sdt", SDT)
+@pytest.mark.parametrize("N", [16, 64, 128, 256])
+@pytest.mark.parametrize("kind", ["single", "varlen"])
+def test_no_write_dtypes(oracle_mod, kind, sdt, N, algo):
+    if kind == "single":
+        case = W.single_token_case(batch=7, heads=6, headdim=80, dstate=N, groups=3, slots=20,
+                                   state_dtype=sdt, pad_frac=0.3, seed=40 + N,
+                                   disable_state_update=True, device=DEV)
+    else:
+        case = W.varlen_case(nseqs=9, max_len=6, heads=4, headdim=80, dstate=N, groups=2,
+                             slots=160, state_dtype=sdt, pad_frac=0.25, seed=50 + N,
+                             disable_state_update=True, device=DEV)
+    r = P.parity(oracle_mod, case, label=f"no-write {kind} {sdt} N={N} {algo}", algorithm=algo)
+    assert r["slots_written"] == 0
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("variant", ["bc_unaligned", "dt_per_dim", "per_channel", "no_z",
+                                     "out_f32", "heads_per_group_odd"])
+@pytest.mark.parametrize("kind", ["single", "varlen"])
+def test_no_write_variants(oracle_mod, kind, variant, algo):
+    """No-write calls through every staging path: element loads of B / C rows
+    off 16-byte alignment, per-row dt' (dt, A, dt_bias per channel), no gate,
+    fp32 y, and a head count per group that CTAs cannot split in 2 or 4."""
+    kw = dict(heads=4, headdim=64, dstate=128, groups=2, state_dtype=torch.bfloat16,
+              disable_state_update=True, device=DEV)
+    if variant == "dt_per_dim":
+        kw["dt_per_dim"] = True
+    if variant == "no_z":
+        kw["with_z"] = False
+    if variant == "heads_per_group_odd":
+        kw.update(heads=6, groups=2)   # 3 heads per group
+    if kind == "single":
+        case = W.single_token_case(batch=9, slots=24, pad_frac=0.2, seed=61, **kw)
+    else:
+        case = W.varlen_case(nseqs=7, max_len=4, slots=80, pad_frac=0.15, seed=62, **kw)
+    if variant == "bc_unaligned":
+        unaligned_bc(case)
+    if variant == "per_channel":
+        g = torch.Generator(device=DEV).manual_seed(8)
+        H, Pd = case.A.shape[0], case.x.shape[-1]
+        case.A = -torch.exp(torch.rand(H, Pd, generator=g, device=DEV) * 2.7)
+        case.D = torch.rand(H, Pd, generator=g, device=DEV)
+        case.dt_bias = -1 - 3 * torch.rand(H, Pd, generator=g, device=DEV)
+    out_dtype = torch.float32 if variant == "out_f32" else None
+    r = P.parity(oracle_mod, case, out_dtype=out_dtype, label=f"no-write {kind} {variant} {algo}",
+                 algorithm=algo)
+    assert r["slots_written"] == 0
+
+
+# ---------------------------------------------------------------------------
 # packed varlen / MTP route
 # ---------------------------------------------------------------------------
 
@@ -156,7 +212,8 @@ def test_varlen_dtypes(oracle_mod, sdt, N, algo):
 @pytest.mark.parametrize("variant", ["empty_seqs", "no_counts", "flat_tables", "dense",
                                      "same_table", "int64", "disable", "no_dst_no_src",
                                      "count_out_of_table", "long_chain", "out_f32",
-                                     "dt_per_dim", "f16_io", "per_channel", "bc_unaligned"])
+                                     "dt_per_dim", "f16_io", "per_channel", "bc_unaligned",
+                                     "disable_long_chain", "disable_dt_per_dim"])
 def test_varlen_variants(oracle_mod, variant, algo):
     kw = dict(nseqs=7, max_len=4, heads=4, headdim=64, dstate=128, groups=2, slots=80,
               state_dtype=torch.float32, pad_frac=0.15, seed=23, device=DEV)
@@ -166,9 +223,11 @@ def test_varlen_variants(oracle_mod, variant, algo):
         kw["same_tables"] = True
     if variant == "int64":
         kw.update(index_dtype=torch.int64, meta_dtype=torch.int64)
-    if variant == "long_chain":
+    if variant in ("long_chain", "disable_long_chain"):
         kw.update(max_len=11, slots=200)   # more steps than one staged group of 4
-    if variant == "dt_per_dim":
+    if variant in ("disable_long_chain", "disable_dt_per_dim"):
+        kw["disable_state_update"] = True
+    if variant in ("dt_per_dim", "disable_dt_per_dim"):
         kw["dt_per_dim"] = True
     if variant == "f16_io":
         kw["io_dtype"] = torch.float16
