@@ -12,11 +12,59 @@
 // sequence, so the slot lookup, the B / C staging and G are done once for
 // all of them, and the next head's tile (contiguous in the slot) is in
 // flight while the current one is computed.
+//
+// With 16-bit state and B / C of the same type, the dot products C_t . h of
+// a tile are one small contraction, [rows x dstate] x [dstate x steps], whose
+// products are exact in 16-bit x 16-bit -> fp32 tensor-core MMA: each warp
+// takes 16 rows with m16n8k16 MMAs (steps padded to 8), the state fragments
+// read by ldmatrix from an XOR-swizzled tile, C_t's fragments built once per
+// CTA.  Elsewhere paired fp32 FMAs and a reduce-scatter over each row's lanes.
 #pragma once
+
+#include <type_traits>
 
 #include "ssu_kernel.cuh"
 
 namespace ssu {
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&a)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+               : "r"(addr));
+}
+
+// d += a b for one m16n8k16 tile (row-major A, column-major B, fp32 accumulate)
+template <class T>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+// two values exactly representable in T, packed low / high
+template <class T>
+__device__ __forceinline__ uint32_t pack_pair(float lo, float hi) {
+  uint32_t w;
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    w = *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    w = *reinterpret_cast<uint32_t*>(&v);
+  }
+  return w;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -380,6 +428,11 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
   constexpr int LEFT = UNR > L::LPR ? UNR / L::LPR : 1;  // rows a lane owns after a reduce
   constexpr bool JOINT = LMAX * UNR == L::LPR;           // one (step, row) sum per lane
   constexpr int TILE_BYTES = ROWS * N * (int)sizeof(ST);
+  // tensor-core dot products: 16-bit state and B / C of one type, 16 rows per
+  // warp, rows of 8 or 16 chunks of 16 bytes (swizzled by row % 8)
+  constexpr bool MMA = sizeof(ST) == 2 && std::is_same<ST, IT>::value && (N == 64 || N == 128) &&
+                       ROWS == 16 * WARPS && LMAX <= 8;
+  constexpr int CHR = N * (int)sizeof(ST) / 16;  // 16-byte chunks per tile row
   constexpr int RAW =
       2 * TILE_BYTES > (int)sizeof(StageT) ? 2 * TILE_BYTES : (int)sizeof(StageT);
   __shared__ __align__(128) unsigned char raw[RAW];  // two state tiles, or a chain's stage
@@ -425,7 +478,12 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
 #pragma unroll 4
       for (int i = threadIdx.x; i < TILE_BYTES / 16; i += THREADS) {
         const bool v = i < valid;
-        cp_async16(dst + i * 16, v ? gsrc + (size_t)i * 16 : static_cast<const char*>(p.state),
+        int o = i * 16;
+        if constexpr (MMA) {  // chunk c of row r at chunk c ^ (r % 8): ldmatrix without conflicts
+          const int r = i / CHR, c = i - r * CHR;
+          o = (r * CHR + (c ^ (r & 7))) * 16;
+        }
+        cp_async16(dst + o, v ? gsrc + (size_t)i * 16 : static_cast<const char*>(p.state),
                    v ? 16 : 0);
       }
     }
@@ -445,7 +503,26 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
   if (tied) stage_head_steps<8, LMAX>(hsteps, p, r0, len, h0, kh);
   __syncthreads();
   pre.finish(hrows[0], p, len, p0, tied, hsteps.dt[0], hsteps.dA[0]);
+  if (kh > 1) pre.load(p, h0 + 1, tied);  // a whole head ahead of its use
   stage_G<N, LMAX, WARPS>(bc, G, len, warp, lane);
+  // C's MMA fragments (B operand, k x n = dstate x step): lane holds columns
+  // k = 16 ks + 8 half + 2 (lane % 4) + {0, 1} of step lane / 4 (zero past len)
+  uint32_t bfr[MMA ? N / 16 : 1][2];
+  if constexpr (MMA) {
+    const int st = lane >> 2, q4 = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < N / 16; ++ks)
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int kc = 16 * ks + 8 * half + 2 * q4;
+        float lo = 0.0f, hi = 0.0f;
+        if (st < len) {
+          lo = bc.C[st][bc_slot<ST, N>(kc)];
+          hi = bc.C[st][bc_slot<ST, N>(kc + 1)];
+        }
+        bfr[ks][half] = pack_pair<ST>(lo, hi);
+      }
+  }
 
   const int q = lane % L::LPR;
   const int rr = lane / L::LPR;
@@ -456,16 +533,27 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
     const unsigned char* tile = raw + (k & 1) * TILE_BYTES;
 
     // 3. ct[t] = C_t . h for this thread's rows: one pass over the tile
-    if (k + 1 < kh) pre.load(p, h0 + k + 1, tied);  // in flight meanwhile
+    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // MMA: rows lane / 4 (+ 8), steps 2 (lane % 4) (+ 1)
+    if constexpr (MMA) {
+      const int arow = warp * 16 + (lane & 15);
+      const uint32_t abase =
+          static_cast<uint32_t>(__cvta_generic_to_shared(tile)) + arow * (CHR * 16);
+#pragma unroll
+      for (int ks = 0; ks < N / 16; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(a, abase + (((2 * ks + (lane >> 4)) ^ (arow & 7)) << 4));
+        mma_16816<ST>(d, a, bfr[ks][0], bfr[ks][1]);
+      }
+    }
     float2 a2[LMAX][UNR];  // even / odd element partial sums
-    if constexpr (!JOINT) {
+    if constexpr (!JOINT && !MMA) {
 #pragma unroll
       for (int t = 0; t < LMAX; ++t)
 #pragma unroll
         for (int u = 0; u < UNR; ++u) a2[t][u] = make_float2(0.0f, 0.0f);
     }
 #pragma unroll
-    for (int c = 0; c < L::CPL; ++c) {
+    for (int c = 0; c < (MMA ? 0 : L::CPL); ++c) {
       float2 cv[LMAX][C2];  // chunk c of every step's C, read once for all rows
 #pragma unroll
       for (int t = 0; t < LMAX; ++t)
@@ -493,7 +581,8 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
     float acc[JOINT ? LMAX * UNR : 1];
     float ct[JOINT ? 1 : LEFT][LMAX];
     int base = 0, plain = 0;
-    if constexpr (JOINT) {
+    if constexpr (MMA) {
+    } else if constexpr (JOINT) {
 #pragma unroll
       for (int t = 0; t < LMAX; ++t)
 #pragma unroll
@@ -515,14 +604,31 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
       }
     }
 
-    // 4. the next head's rows; then the tile buffer goes to head k + 2
+    // 4. the next head's rows (loaded one iteration ago) and the loads of the
+    //    one after; then the tile buffer goes to head k + 2
     if (k + 1 < kh)
       pre.finish(hrows[(k + 1) & 1], p, len, p0, tied, hsteps.dt[k + 1], hsteps.dA[k + 1]);
+    if (k + 2 < kh) pre.load(p, h0 + k + 2, tied);
     __syncthreads();  // every thread is done with tile k; hrows[(k + 1) & 1] complete
     issue_tile(k + 2, k & 1);
 
     // 5. y of head k
-    if constexpr (JOINT) {
+    if constexpr (MMA) {
+      // lanes with lane % 4 >= 2 hold only padded steps (4..7): they take
+      // over row + 8 of lane - 2, so every lane forms two y of one row
+      const float u0 = __shfl_up_sync(0xffffffffu, d[2], 2);
+      const float u1 = __shfl_up_sync(0xffffffffu, d[3], 2);
+      const bool hi = (lane & 2) != 0;
+      const int t = 2 * (lane & 1);
+      const int j = warp * 16 + (lane >> 2) + (hi ? 8 : 0);
+      const float c0 = hi ? u0 : d[0], c1 = hi ? u1 : d[1];
+      if (p0 + j < p.P) {
+        if (t < len)
+          closed_form_y_step<IT, LMAX>(p, hrows[k & 1], G, c0, t, j, h0 + k, p0 + j, r0);
+        if (t + 1 < len)
+          closed_form_y_step<IT, LMAX>(p, hrows[k & 1], G, c1, t + 1, j, h0 + k, p0 + j, r0);
+      }
+    } else if constexpr (JOINT) {
       const int t = base / UNR, u = base - t * UNR;
       const int j = jbase + u * L::RPW;
       if (t < len && p0 + j < p.P)

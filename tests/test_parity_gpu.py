@@ -163,12 +163,14 @@ def test_no_write_dtypes(oracle_mod, kind, sdt, N, algo):
 
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("variant", ["bc_unaligned", "dt_per_dim", "per_channel", "no_z",
-                                     "out_f32", "heads_per_group_odd"])
+                                     "out_f32", "heads_per_group_odd", "f16_state_f16_io",
+                                     "dstate64", "ragged_rows"])
 @pytest.mark.parametrize("kind", ["single", "varlen"])
 def test_no_write_variants(oracle_mod, kind, variant, algo):
     """No-write calls through every staging path: element loads of B / C rows
     off 16-byte alignment, per-row dt' (dt, A, dt_bias per channel), no gate,
-    fp32 y, and a head count per group that CTAs cannot split in 2 or 4."""
+    fp32 y, a head count per group that CTAs cannot split in 2 or 4, the
+    fp16 tensor-core path, dstate 64 and a headdim that leaves a ragged tile."""
     kw = dict(heads=4, headdim=64, dstate=128, groups=2, state_dtype=torch.bfloat16,
               disable_state_update=True, device=DEV)
     if variant == "dt_per_dim":
@@ -177,6 +179,12 @@ def test_no_write_variants(oracle_mod, kind, variant, algo):
         kw["with_z"] = False
     if variant == "heads_per_group_odd":
         kw.update(heads=6, groups=2)   # 3 heads per group
+    if variant == "f16_state_f16_io":
+        kw.update(state_dtype=torch.float16, io_dtype=torch.float16)
+    if variant == "dstate64":
+        kw["dstate"] = 64
+    if variant == "ragged_rows":
+        kw.update(headdim=80, heads=16, groups=2)  # 8 heads per group, a 16-row tail tile
     if kind == "single":
         case = W.single_token_case(batch=9, slots=24, pad_frac=0.2, seed=61, **kw)
     else:
