@@ -156,6 +156,10 @@ ssu_status check_params(const ssu_params* p, ssu::KParams* k) {
     k->bc_vec16 = a16(p->B) && a16(p->C) && p->B_row_stride % 8 == 0 &&
                   p->B_group_stride % 8 == 0 && p->C_row_stride % 8 == 0 &&
                   p->C_group_stride % 8 == 0;
+    k->xz_vec16 = a16(p->x) && p->x_row_stride % 8 == 0 && p->x_head_stride % 8 == 0 &&
+                  (!p->z || (a16(p->z) && p->z_row_stride % 8 == 0 &&
+                             p->z_head_stride % 8 == 0)) &&
+                  p->headdim % 8 == 0;
   }
   k->A = p->A;
   k->A_s = p->A_stride;

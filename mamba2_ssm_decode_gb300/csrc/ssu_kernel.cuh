@@ -82,6 +82,7 @@ struct KParams {
   int softplus;
   int disable;
   int bc_vec16;  // B and C rows start on 16-byte boundaries (pointer and strides)
+  int xz_vec16;  // so do x and z rows, and headdim is a multiple of 8
   int64_t pad;
   FastDiv fd_tiles, fd_H, fd_hr;  // divisions by tiles, H and heads per group
 };

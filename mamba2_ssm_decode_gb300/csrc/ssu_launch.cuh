@@ -156,11 +156,10 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
                          int64_t nitems, cudaStream_t stream, int algorithm) {
   using T = Tune<ST, N>;
   using Cfg = SSUConfig<ST, IT, N, T::WARPS, T::UNR, T::LMAX>;
-  // auto (the fastest as measured): the bulk-copy pipeline for one-token calls,
-  // except 16-bit state with no state written (the no-write kernel); the
-  // register kernel for multi-token chains, the no-write kernel for those
-  // that write no state
-  const bool auto_bulk = !varlen && (!p.disable || sizeof(ST) == 4);
+  // auto (the fastest as measured): the bulk-copy pipeline for one-token calls
+  // that write state, the register kernel for multi-token chains that do, the
+  // no-write kernel for every call that writes none
+  const bool auto_bulk = !varlen && !p.disable;
   const bool bulk = algorithm == 2 /* SSU_ALGO_BULK */ || (algorithm == 0 && auto_bulk);
   if (bulk) {
     const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};

@@ -184,47 +184,82 @@ __device__ __forceinline__ void stage_head_steps(HeadSteps<KMAX, LMAX>& s, const
 // The per-row scalars of one head in two halves, so that the loads of the
 // next head are in flight while the current head computes: load() issues
 // this thread's global loads into registers, finish() evaluates and stores
-// them.  Thread i keeps step i % LMAX of rows i / LMAX + m THREADS / LMAX;
-// their x / z offsets within a head are fixed, so they are formed once.
+// them.  Vector form (dt, A, D, dt_bias per head, x / z rows 16-byte
+// aligned): task i < LMAX ROWS / 8 takes step i / (ROWS / 8) of 8 rows, with
+// one 16-byte load of x and one of z.  Otherwise thread i keeps step i % LMAX
+// of rows i / LMAX + m THREADS / LMAX, element by element.
 template <class IT, int ROWS, int LMAX, int THREADS>
 struct RowPrefetch {
-  static_assert(THREADS % LMAX == 0, "a thread keeps one step");
+  static_assert(THREADS % LMAX == 0 && ROWS % 8 == 0, "row layout");
   static constexpr int NP = (ROWS * LMAX + THREADS - 1) / THREADS;  // rows per thread
-  float x[NP], z[NP], D[NP], dt[NP], A[NP], bias[NP];
+  static constexpr int VT = LMAX * (ROWS / 8);                       // vector tasks
+  static constexpr int WN = 6 * NP > 9 ? 6 * NP : 9;
+  uint32_t w[WN];  // vector: x (8), z (8), D; elementwise: x, z, D, dt, A, dt_bias per row
   int64_t xo[NP], zo[NP];
   int prow[NP];
   int t;
   int64_t r;  // packed row of step t
+  bool vec;
 
-  __device__ __forceinline__ void init(const KParams& p, int64_t r0, int n, int p0) {
+  __device__ __forceinline__ void init(const KParams& p, int64_t r0, int n, int p0, bool v) {
+    vec = v;
+    if (vec) {
+      const int i = threadIdx.x;
+      t = i / (ROWS / 8);
+      const int j = (i - t * (ROWS / 8)) * 8;
+      r = r0 + t;
+      prow[0] = (i < VT && t < n && p0 + j < p.P) ? p0 + j : -1;
+      xo[0] = r * p.x_rs + prow[0];
+      zo[0] = r * p.z_rs + prow[0];
+      return;
+    }
     t = threadIdx.x % LMAX;
     r = r0 + t;
 #pragma unroll
     for (int m = 0; m < NP; ++m) {
       const int j = threadIdx.x / LMAX + m * (THREADS / LMAX);
       prow[m] = (t < n && j < ROWS && p0 + j < p.P) ? p0 + j : -1;
-      xo[m] = (r0 + t) * p.x_rs + prow[m];
-      zo[m] = (r0 + t) * p.z_rs + prow[m];
+      xo[m] = r * p.x_rs + prow[m];
+      zo[m] = r * p.z_rs + prow[m];
     }
   }
 
   __device__ __forceinline__ void load(const KParams& p, int h, bool tied) {
     const IT* xp = static_cast<const IT*>(p.x);
     const IT* zp = static_cast<const IT*>(p.z);
+    if (vec) {
+      if (prow[0] >= 0) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xp + xo[0] + (int64_t)h * p.x_hs));
+        w[0] = xv.x, w[1] = xv.y, w[2] = xv.z, w[3] = xv.w;
+        if (zp) {
+          const uint4 zv =
+              __ldg(reinterpret_cast<const uint4*>(zp + zo[0] + (int64_t)h * p.z_hs));
+          w[4] = zv.x, w[5] = zv.y, w[6] = zv.z, w[7] = zv.w;
+        }
+        w[8] = __float_as_uint(p.D ? p.D[(int64_t)h * p.D_s] : 0.0f);
+      }
+      return;
+    }
 #pragma unroll
     for (int m = 0; m < NP; ++m) {
-      x[m] = z[m] = D[m] = dt[m] = A[m] = bias[m] = 0.0f;
+      float x = 0.0f, z = 0.0f, D = 0.0f, dt = 0.0f, A = 0.0f, bias = 0.0f;
       if (prow[m] >= 0) {
-        x[m] = io_to_float<IT>(xp[xo[m] + (int64_t)h * p.x_hs]);
-        if (zp) z[m] = io_to_float<IT>(zp[zo[m] + (int64_t)h * p.z_hs]);
-        if (p.D) D[m] = p.D[(int64_t)h * p.D_s + (int64_t)prow[m] * p.D_ds];
+        x = io_to_float<IT>(xp[xo[m] + (int64_t)h * p.x_hs]);
+        if (zp) z = io_to_float<IT>(zp[zo[m] + (int64_t)h * p.z_hs]);
+        if (p.D) D = p.D[(int64_t)h * p.D_s + (int64_t)prow[m] * p.D_ds];
         if (!tied) {
-          dt[m] = p.dt[r * p.dt_rs + (int64_t)h * p.dt_hs + (int64_t)prow[m] * p.dt_ds];
-          A[m] = p.A[(int64_t)h * p.A_s + (int64_t)prow[m] * p.A_ds];
+          dt = p.dt[r * p.dt_rs + (int64_t)h * p.dt_hs + (int64_t)prow[m] * p.dt_ds];
+          A = p.A[(int64_t)h * p.A_s + (int64_t)prow[m] * p.A_ds];
           if (p.dt_bias)
-            bias[m] = p.dt_bias[(int64_t)h * p.bias_s + (int64_t)prow[m] * p.bias_ds];
+            bias = p.dt_bias[(int64_t)h * p.bias_s + (int64_t)prow[m] * p.bias_ds];
         }
       }
+      w[6 * m + 0] = __float_as_uint(x);
+      w[6 * m + 1] = __float_as_uint(z);
+      w[6 * m + 2] = __float_as_uint(D);
+      w[6 * m + 3] = __float_as_uint(dt);
+      w[6 * m + 4] = __float_as_uint(A);
+      w[6 * m + 5] = __float_as_uint(bias);
     }
   }
 
@@ -232,6 +267,37 @@ struct RowPrefetch {
   template <class HR>
   __device__ __forceinline__ void finish(HR& s, const KParams& p, int n, int p0, bool tied,
                                          const float* hdt, const float* hdA) const {
+    if (vec) {
+      if (prow[0] < 0) return;
+      const int j0 = prow[0] - p0;
+      const float dtv = hdt[t], dA = hdA[t], D = __uint_as_float(w[8]);
+      const IT* xe = reinterpret_cast<const IT*>(&w[0]);
+      const IT* ze = reinterpret_cast<const IT*>(&w[4]);
+      float dtx[8], Dx[8], gate[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float xv = io_to_float<IT>(xe[e]);
+        dtx[e] = dtv * xv;
+        Dx[e] = D * xv;
+        gate[e] = 1.0f;
+        if (p.z) {
+          const float zv = io_to_float<IT>(ze[e]);
+          gate[e] = __fdividef(zv, 1.0f + __expf(-zv));
+        }
+      }
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {
+        const int o = j0 + 4 * hq;
+        *reinterpret_cast<float4*>(&s.dA[t][o]) = make_float4(dA, dA, dA, dA);
+        *reinterpret_cast<float4*>(&s.dtx[t][o]) =
+            make_float4(dtx[4 * hq], dtx[4 * hq + 1], dtx[4 * hq + 2], dtx[4 * hq + 3]);
+        *reinterpret_cast<float4*>(&s.Dx[t][o]) =
+            make_float4(Dx[4 * hq], Dx[4 * hq + 1], Dx[4 * hq + 2], Dx[4 * hq + 3]);
+        *reinterpret_cast<float4*>(&s.gate[t][o]) =
+            make_float4(gate[4 * hq], gate[4 * hq + 1], gate[4 * hq + 2], gate[4 * hq + 3]);
+      }
+      return;
+    }
     if (t >= n) return;
 #pragma unroll
     for (int m = 0; m < NP; ++m) {
@@ -239,18 +305,19 @@ struct RowPrefetch {
       if (j >= ROWS) break;
       float dAv = 1.0f, dtx = 0.0f, Dx = 0.0f, gate = 1.0f;
       if (prow[m] >= 0) {
+        const float x = __uint_as_float(w[6 * m + 0]), z = __uint_as_float(w[6 * m + 1]);
         float dtv;
         if (tied) {
           dtv = hdt[t];
           dAv = hdA[t];
         } else {
-          dtv = dt[m] + bias[m];
+          dtv = __uint_as_float(w[6 * m + 3]) + __uint_as_float(w[6 * m + 5]);
           if (p.softplus) dtv = softplus_f(dtv);
-          dAv = expf(A[m] * dtv);
+          dAv = expf(__uint_as_float(w[6 * m + 4]) * dtv);
         }
-        dtx = dtv * x[m];
-        Dx = D[m] * x[m];
-        if (p.z) gate = __fdividef(z[m], 1.0f + __expf(-z[m]));
+        dtx = dtv * x;
+        Dx = __uint_as_float(w[6 * m + 2]) * x;
+        if (p.z) gate = __fdividef(z, 1.0f + __expf(-z));
       }
       s.dA[t][j] = dAv;
       s.dtx[t][j] = dtx;
@@ -497,7 +564,7 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
   const int warp = threadIdx.x >> 5;
   const bool tied = per_head_dt(p);
   RowPrefetch<IT, ROWS, LMAX, THREADS> pre;
-  pre.init(p, r0, len, p0);
+  pre.init(p, r0, len, p0, tied && p.xz_vec16 && (!p.D || p.D_ds == 0));
   pre.load(p, h0, tied);
   stage_bc<ST, IT, N, LMAX, THREADS>(bc, p, r0, 0, len, (int)p.fd_hr.div((uint32_t)h0));
   if (tied) stage_head_steps<8, LMAX>(hsteps, p, r0, len, h0, kh);

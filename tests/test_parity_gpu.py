@@ -105,6 +105,17 @@ def test_one_token_variants(oracle_mod, variant, algo):
     P.parity(oracle_mod, case, out_dtype=out_dtype, label=variant, algorithm=algo)
 
 
+def unaligned_xz(case):
+    """Move x and z to odd element offsets (rows not 16-byte aligned)."""
+    for name in ("x", "z"):
+        t = getattr(case, name)
+        R = t.shape[0]
+        big = torch.zeros(R, t[0].numel() + 1, dtype=t.dtype, device=t.device)
+        v = big[:, 1:].view(t.shape)
+        v.copy_(t)
+        setattr(case, name, v)
+
+
 def unaligned_bc(case):
     """Move B and C into one buffer at odd element offsets (rows not 16-byte aligned)."""
     R, G, N = case.B.shape
@@ -164,7 +175,7 @@ def test_no_write_dtypes(oracle_mod, kind, sdt, N, algo):
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("variant", ["bc_unaligned", "dt_per_dim", "per_channel", "no_z",
                                      "out_f32", "heads_per_group_odd", "f16_state_f16_io",
-                                     "dstate64", "ragged_rows"])
+                                     "dstate64", "ragged_rows", "xz_unaligned"])
 @pytest.mark.parametrize("kind", ["single", "varlen"])
 def test_no_write_variants(oracle_mod, kind, variant, algo):
     """No-write calls through every staging path: element loads of B / C rows
@@ -191,6 +202,8 @@ def test_no_write_variants(oracle_mod, kind, variant, algo):
         case = W.varlen_case(nseqs=7, max_len=4, slots=80, pad_frac=0.15, seed=62, **kw)
     if variant == "bc_unaligned":
         unaligned_bc(case)
+    if variant == "xz_unaligned":
+        unaligned_xz(case)
     if variant == "per_channel":
         g = torch.Generator(device=DEV).manual_seed(8)
         H, Pd = case.A.shape[0], case.x.shape[-1]
