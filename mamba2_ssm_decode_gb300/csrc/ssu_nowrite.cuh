@@ -186,8 +186,8 @@ __device__ __forceinline__ void stage_head_steps(HeadSteps<KMAX, LMAX>& s, const
 // this thread's global loads into registers, finish() evaluates and stores
 // them.  Vector form (dt, A, D, dt_bias per head, x / z rows 16-byte
 // aligned): task i < LMAX ROWS / 8 takes step i / (ROWS / 8) of 8 rows, with
-// one 16-byte load of x and one of z.  Otherwise thread i keeps step i % LMAX
-// of rows i / LMAX + m THREADS / LMAX, element by element.
+// one 16-byte load of x and one of z.  Otherwise, with T = THREADS / LMAX,
+// thread i keeps step i / T of rows i % T + m T, element by element.
 template <class IT, int ROWS, int LMAX, int THREADS>
 struct RowPrefetch {
   static_assert(THREADS % LMAX == 0 && ROWS % 8 == 0, "row layout");
@@ -213,11 +213,11 @@ struct RowPrefetch {
       zo[0] = r * p.z_rs + prow[0];
       return;
     }
-    t = threadIdx.x % LMAX;
+    t = threadIdx.x / (THREADS / LMAX);
     r = r0 + t;
 #pragma unroll
     for (int m = 0; m < NP; ++m) {
-      const int j = threadIdx.x / LMAX + m * (THREADS / LMAX);
+      const int j = threadIdx.x - t * (THREADS / LMAX) + m * (THREADS / LMAX);
       prow[m] = (t < n && j < ROWS && p0 + j < p.P) ? p0 + j : -1;
       xo[m] = r * p.x_rs + prow[m];
       zo[m] = r * p.z_rs + prow[m];
@@ -301,7 +301,7 @@ struct RowPrefetch {
     if (t >= n) return;
 #pragma unroll
     for (int m = 0; m < NP; ++m) {
-      const int j = threadIdx.x / LMAX + m * (THREADS / LMAX);
+      const int j = threadIdx.x - t * (THREADS / LMAX) + m * (THREADS / LMAX);
       if (j >= ROWS) break;
       float dAv = 1.0f, dtx = 0.0f, Dx = 0.0f, gate = 1.0f;
       if (prow[m] >= 0) {
