@@ -1,17 +1,18 @@
-// ssu_nowrite.cuh -- the SSU for calls that write no state
-// (disable_state_update).
+// ssu_headrun.cuh -- head-run kernels: one CTA takes a run of heads of one
+// group for one sequence (and one row tile), so the slot lookup, the B / C
+// staging and the per-head dt' / dA are done once for the run, and the state
+// tiles of the next heads (contiguous in the slot) land in shared memory by
+// cp.async while the current head computes.  Two kernels: packed chains that
+// write state (ssu_run_kernel, exactly the register kernel's steps per head),
+// and calls that write no state (ssu_nowrite_kernel, below).
 //
-// With no state to store, the steps of a staged chunk have a closed form.
+// Calls that write no state: the steps of a staged chunk have a closed form.
 // Unrolling h_t = dA_t h_{t-1} + dtx_t B_t from the chunk's initial state h:
 //   C_t . h_t = P_t (C_t . h) + sum_{s <= t} E_{s,t} (C_t . B_s),
 //   P_t = dA_0 dA_1 ... dA_t,   E_{s,t} = dtx_s dA_{s+1} ... dA_t.
 // A state element then costs one FMA per step (the dot products C_t . h)
 // instead of three, the products G[t][s] = C_t . B_s are formed once per
-// CTA, and the state never has to sit in registers: it lands in shared
-// memory by cp.async.  A CTA takes several heads of one group for one
-// sequence, so the slot lookup, the B / C staging and G are done once for
-// all of them, and the next head's tile (contiguous in the slot) is in
-// flight while the current one is computed.
+// CTA, and the state never has to sit in registers.
 //
 // With 16-bit state and B / C of the same type, the dot products C_t . h of
 // a tile are one small contraction, [rows x dstate] x [dstate x steps], whose
@@ -263,8 +264,16 @@ struct RowPrefetch {
     }
   }
 
+  // silu(z): the fast exp / division intrinsics (FAST) or the exact forms the
+  // state-writing kernels share bit for bit
+  template <bool FAST>
+  __device__ __forceinline__ static float silu(float z) {
+    if constexpr (FAST) return __fdividef(z, 1.0f + __expf(-z));
+    else return z / (1.0f + expf(-z));
+  }
+
   // hdt / hdA: this head's per-head dt' and dA by step (used when tied)
-  template <class HR>
+  template <bool FAST, class HR>
   __device__ __forceinline__ void finish(HR& s, const KParams& p, int n, int p0, bool tied,
                                          const float* hdt, const float* hdA) const {
     if (vec) {
@@ -280,10 +289,7 @@ struct RowPrefetch {
         dtx[e] = dtv * xv;
         Dx[e] = D * xv;
         gate[e] = 1.0f;
-        if (p.z) {
-          const float zv = io_to_float<IT>(ze[e]);
-          gate[e] = __fdividef(zv, 1.0f + __expf(-zv));
-        }
+        if (p.z) gate[e] = silu<FAST>(io_to_float<IT>(ze[e]));
       }
 #pragma unroll
       for (int hq = 0; hq < 2; ++hq) {
@@ -317,7 +323,7 @@ struct RowPrefetch {
         }
         dtx = dtv * x;
         Dx = __uint_as_float(w[6 * m + 2]) * x;
-        if (p.z) gate = __fdividef(z, 1.0f + __expf(-z));
+        if (p.z) gate = silu<FAST>(z);
       }
       s.dA[t][j] = dAv;
       s.dtx[t][j] = dtx;
@@ -569,7 +575,7 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
   stage_bc<ST, IT, N, LMAX, THREADS>(bc, p, r0, 0, len, (int)p.fd_hr.div((uint32_t)h0));
   if (tied) stage_head_steps<8, LMAX>(hsteps, p, r0, len, h0, kh);
   __syncthreads();
-  pre.finish(hrows[0], p, len, p0, tied, hsteps.dt[0], hsteps.dA[0]);
+  pre.finish<true>(hrows[0], p, len, p0, tied, hsteps.dt[0], hsteps.dA[0]);
   if (kh > 1) pre.load(p, h0 + 1, tied);  // a whole head ahead of its use
   stage_G<N, LMAX, WARPS>(bc, G, len, warp, lane);
   // C's MMA fragments (B operand, k x n = dstate x step): lane holds columns
@@ -674,7 +680,7 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
     // 4. the next head's rows (loaded one iteration ago) and the loads of the
     //    one after; then the tile buffer goes to head k + 2
     if (k + 1 < kh)
-      pre.finish(hrows[(k + 1) & 1], p, len, p0, tied, hsteps.dt[k + 1], hsteps.dA[k + 1]);
+      pre.finish<true>(hrows[(k + 1) & 1], p, len, p0, tied, hsteps.dt[k + 1], hsteps.dA[k + 1]);
     if (k + 2 < kh) pre.load(p, h0 + k + 2, tied);
     __syncthreads();  // every thread is done with tile k; hrows[(k + 1) & 1] complete
     issue_tile(k + 2, k & 1);
@@ -706,6 +712,167 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
         const int j = jbase + (base + i) * L::RPW;
         if (p0 + j < p.P)
           closed_form_y<IT, LMAX>(p, hrows[k & 1], G, ct[i], len, j, h0 + k, p0 + j, r0);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the same head runs for packed chains that write state
+// ---------------------------------------------------------------------------
+
+// The stage as step_rows reads it, assembled from the run's shared pieces.
+template <int N, int ROWS, int LMAX>
+struct StageView {
+  const float (*B)[N];
+  const float (*C)[N];
+  const float (*dA)[ROWS];
+  const float (*dtx)[ROWS];
+  const float (*Dx)[ROWS];
+  const float (*gate)[ROWS];
+};
+
+// Packed chains that write state: grid (row tiles, runs of kh heads of one
+// group, sequences).  The slot lookups, the chain's write slots, B / C and
+// the per-head dt' / dA table are formed once for the run; each head's state
+// tile lands in shared memory by cp.async (the next two in flight while one
+// computes); each head then runs exactly the steps of the register kernel
+// (step_rows, the same staged values and stores, so the same bits).  Chains
+// longer than LMAX take the register kernel's block, head by head.
+template <class ST, class IT, int N, int WARPS, int UNR, int LMAX>
+__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
+    ssu_run_kernel(const KParams p, const VarlenArgs va, int64_t seq0, int kh) {
+  using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
+  using L = typename Cfg::L;
+  constexpr int ROWS = Cfg::ROWS;
+  constexpr int THREADS = Cfg::THREADS;
+  using StageT = Stage<N, ROWS, LMAX>;
+  constexpr int TILE_BYTES = ROWS * N * (int)sizeof(ST);
+  constexpr int RAW =
+      2 * TILE_BYTES > (int)sizeof(StageT) ? 2 * TILE_BYTES : (int)sizeof(StageT);
+  __shared__ __align__(128) unsigned char raw[RAW];  // two state tiles, or a chain's stage
+  __shared__ StepsBC<N, LMAX> bc;
+  __shared__ HeadRows<ROWS, LMAX> hrows[2];
+  __shared__ HeadSteps<8, LMAX> hsteps;
+
+  const int64_t s = seq0 + blockIdx.z;
+  const int h0 = (int)blockIdx.y * kh;
+  const int p0 = (int)blockIdx.x * ROWS;
+  int64_t r0, src;
+  int len;
+  bool read_ok;
+  if (!varlen_item(p, va, s, &r0, &len, &src, &read_ok)) return;
+  const TableArgs dtab = va.dst.idx ? va.dst : va.src;  // no write table: the read table
+  const int idx64 = va.idx64;
+  auto dst_of = [dtab, idx64, s](int t, int64_t* o) -> bool {
+    if (dtab.idx) return table_entry(dtab, s, t, idx64, o);
+    *o = s;
+    return true;
+  };
+  if (len > LMAX) {
+    StageT& stg = *reinterpret_cast<StageT*>(raw);
+    for (int k = 0; k < kh; ++k) {
+      ssu_block_on<ST, IT, N, WARPS, UNR, LMAX>(stg, p, h0 + k, p0, r0, len, src, read_ok,
+                                                dst_of);
+      __syncthreads();  // the stage is free for the next head
+    }
+    return;
+  }
+
+  // the chain's write slots (the same for every head of the run)
+  int64_t dsts[LMAX];
+  bool dok[LMAX];
+#pragma unroll
+  for (int i = 0; i < LMAX; ++i) {
+    int64_t v = -1;
+    dok[i] = i < len && read_ok && !p.disable && dst_of(i, &v) && slot_ok(v, p.pad, p.slots);
+    dsts[i] = v;
+  }
+
+  // 1. state tiles of the first two heads by 16-byte async copies
+  const int64_t block_elems = (int64_t)p.P * N;
+  const int nrows = p.P - p0 < ROWS ? p.P - p0 : ROWS;
+  const int valid = read_ok ? nrows * N * (int)sizeof(ST) / 16 : 0;
+  const char* slot_rows = reinterpret_cast<const char*>(
+      static_cast<const ST*>(p.state) + (read_ok ? src : 0) * p.H * block_elems +
+      (int64_t)p0 * N);
+  auto issue_tile = [&](int k, int buf) {
+    if (k < kh) {
+      const char* gsrc = slot_rows + (size_t)(h0 + k) * block_elems * sizeof(ST);
+      unsigned char* dst = raw + buf * TILE_BYTES;
+#pragma unroll 4
+      for (int i = threadIdx.x; i < TILE_BYTES / 16; i += THREADS) {
+        const bool v = i < valid;
+        cp_async16(dst + i * 16, v ? gsrc + (size_t)i * 16 : static_cast<const char*>(p.state),
+                   v ? 16 : 0);
+      }
+    }
+    cp_async_commit();
+  };
+  issue_tile(0, 0);
+  issue_tile(1, 1);
+
+  // 2. B / C, the per-head dt' / dA table and the first head's rows
+  const bool tied = per_head_dt(p);
+  RowPrefetch<IT, ROWS, LMAX, THREADS> pre;
+  pre.init(p, r0, len, p0, tied && p.xz_vec16 && (!p.D || p.D_ds == 0));
+  pre.load(p, h0, tied);
+  stage_bc<ST, IT, N, LMAX, THREADS>(bc, p, r0, 0, len, (int)p.fd_hr.div((uint32_t)h0));
+  if (tied) stage_head_steps<8, LMAX>(hsteps, p, r0, len, h0, kh);
+  __syncthreads();
+  pre.finish<false>(hrows[0], p, len, p0, tied, hsteps.dt[0], hsteps.dA[0]);
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int q = lane % L::LPR;
+  const int rr = lane / L::LPR;
+  const int jbase = warp * UNR * L::RPW + rr;
+  ST* state = static_cast<ST*>(p.state);
+  for (int k = 0; k < kh; ++k) {
+    cp_async_wait<1>();  // head k's copies (the newest group is head k + 1's)
+    __syncthreads();     // ... from every thread; hrows[k & 1] complete
+    const int h = h0 + k;
+    // 3. this thread's state chunks of head k, widened to fp32
+    float2 hs[UNR][L::EPL / 2];
+    {
+      const unsigned char* tile = raw + (k & 1) * TILE_BYTES;
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int j = jbase + u * L::RPW;
+#pragma unroll
+        for (int c = 0; c < L::CPL; ++c)
+          Elem<ST>::unpack2(*reinterpret_cast<const uint4*>(
+                                tile + ((size_t)j * N + (q + c * L::LPR) * L::VEC) * sizeof(ST)),
+                            &hs[u][c * L::VEC / 2]);
+      }
+    }
+    __syncthreads();  // every thread has its chunks: the buffer goes to head k + 2
+    issue_tile(k + 2, k & 1);
+    // 4. the next head's rows (into the other buffer)
+    if (k + 1 < kh) {
+      pre.load(p, h + 1, tied);
+      pre.finish<false>(hrows[(k + 1) & 1], p, len, p0, tied, hsteps.dt[k + 1],
+                        hsteps.dA[k + 1]);
+    }
+    // 5. the steps of head k, each step's state to its write slot
+    const StageView<N, ROWS, LMAX> view{bc.B, bc.C, hrows[k & 1].dA, hrows[k & 1].dtx,
+                                        hrows[k & 1].Dx, hrows[k & 1].gate};
+#pragma unroll
+    for (int tt = 0; tt < LMAX; ++tt) {
+      if (tt >= len) break;
+      step_rows<ST, IT, N, UNR>(hs, view, tt, q, jbase, p, h, p0, r0 + tt);
+      if (dok[tt]) {
+        ST* base = state + ((dsts[tt] * p.H + h) * block_elems);
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          const int prow = p0 + (warp * UNR + u) * L::RPW + rr;
+          if (prow < p.P) {
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c)
+              st_state(base + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
+                       Elem<ST>::pack2(&hs[u][c * L::VEC / 2]));
+          }
+        }
       }
     }
   }

@@ -431,14 +431,15 @@ __device__ __forceinline__ void stage_steps(Stage<N, ROWS, LMAX>& s, const KPara
 
 // One CTA: rows [p0, p0 + ROWS) of head h, sequence rows [r0, r0 + len),
 // state read from `src` (if read_ok), step t written to dst_of(t).
-template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, class DstFn>
-__device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64_t r0, int len,
-                                          int64_t src, bool read_ok, DstFn dst_of) {
+// (with the stage in caller-provided shared memory)
+template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, class DstFn, class StageT>
+__device__ __forceinline__ void ssu_block_on(StageT& stg, const KParams& p, int h, int p0,
+                                             int64_t r0, int len, int64_t src, bool read_ok,
+                                             DstFn dst_of) {
   using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
   using L = typename Cfg::L;
   constexpr int ROWS = Cfg::ROWS;
   constexpr int THREADS = Cfg::THREADS;
-  __shared__ Stage<N, ROWS, LMAX> stg;
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -541,6 +542,13 @@ __device__ __forceinline__ bool varlen_item(const KParams& p, const VarlenArgs& 
   return true;
 }
 
+template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, class DstFn>
+__device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64_t r0, int len,
+                                          int64_t src, bool read_ok, DstFn dst_of) {
+  __shared__ Stage<N, SSUConfig<ST, IT, N, WARPS, UNR, LMAX>::ROWS, LMAX> stg;
+  ssu_block_on<ST, IT, N, WARPS, UNR, LMAX>(stg, p, h, p0, r0, len, src, read_ok, dst_of);
+}
+
 // One-token decode: blockIdx -> (sequence b, head, row tile).
 template <class ST, class IT, int N, int WARPS, int UNR>
 __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
@@ -556,51 +564,6 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
   const int64_t dst = a.dsbi ? load_int(a.dsbi, b, a.idx64) : src;
   ssu_block<ST, IT, N, WARPS, UNR, 1>(p, h, p0, b, 1, src, read_ok,
                                       [dst](int, int64_t* o) { *o = dst; return true; });
-}
-
-// Packed varlen / MTP: blockIdx -> (sequence s, head, row tile).
-template <class ST, class IT, int N, int WARPS, int UNR, int LMAX>
-__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
-    ssu_varlen_kernel(const KParams p, const VarlenArgs a) {
-  // Plain divisions (once per CTA): at this kernel's 128-register cap the
-  // fast-division form made the register allocation spill more, and measured
-  // slower.
-  const int tile = (int)(blockIdx.x % p.tiles);
-  const int64_t rest = blockIdx.x / p.tiles;
-  const int h = (int)(rest % p.H);
-  const int64_t s = rest / p.H;
-  using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
-  const int p0 = tile * Cfg::ROWS;
-
-  int64_t begin, end;
-  if (a.cu) {
-    begin = load_int(a.cu, s, a.meta64);
-    end = load_int(a.cu, s + 1, a.meta64);
-  } else {
-    begin = s * a.dense_steps;
-    end = begin + a.dense_steps;
-  }
-  if (begin < 0) begin = 0;
-  if (end > a.rows) end = a.rows;
-  if (end <= begin) return;  // uniform over the CTA: an empty sequence does nothing
-  const int len = (int)(end - begin);
-
-  int64_t src = s;
-  bool read_ok = true;
-  if (a.src.idx) {
-    const int64_t col = a.na ? load_int(a.na, s, a.meta64) - 1 : 0;
-    read_ok = table_entry(a.src, s, col, a.idx64, &src);
-  }
-  read_ok = read_ok && slot_ok(src, p.pad, p.slots);
-
-  const TableArgs dtab = a.dst.idx ? a.dst : a.src;  // no write table: the read table
-  const int idx64 = a.idx64;
-  auto dst_of = [dtab, idx64, s](int t, int64_t* o) -> bool {
-    if (dtab.idx) return table_entry(dtab, s, t, idx64, o);
-    *o = s;
-    return true;
-  };
-  ssu_block<ST, IT, N, WARPS, UNR, LMAX>(p, h, p0, begin, len, src, read_ok, dst_of);
 }
 
 }  // namespace ssu

@@ -4,7 +4,7 @@
 #include <algorithm>
 
 #include "ssu_bulk.cuh"
-#include "ssu_nowrite.cuh"
+#include "ssu_headrun.cuh"
 
 namespace ssu {
 
@@ -41,6 +41,15 @@ struct NoWriteTune {
       1, cmin(Tune<ST, N>::UNR, 16384 / (WARPS * L::RPW * N * (int)sizeof(ST))));
   static constexpr int ROWS = WARPS * L::RPW * UNR;
 };
+
+// Heads per CTA of the head-run kernels: the largest of 8, 4, 2, 1 dividing
+// the heads per group that still leaves at least 4096 CTAs (several waves of
+// resident CTAs, so the last one is a small share of the launch).
+inline int heads_per_cta(int hr, int64_t ctas_one_head_each) {
+  for (int kh = 8; kh > 1; kh /= 2)
+    if (hr % kh == 0 && ctas_one_head_each / kh >= 4096) return kh;
+  return 1;
+}
 
 // Bulk-copy pipeline shape: CW consumer warps, each thread owning UNR state
 // rows (capped so a tile has at most 64 rows), plus one producer warp; as
@@ -168,29 +177,44 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
                   : launch_bulk<ST, IT, N, false>(p, o0, v0, nitems, stream);
   }
   if (nitems <= 0) return cudaSuccess;
-  if (p.disable) {
-    // no-write kernel: grid (row tiles, runs of kh heads of one group,
-    // sequences); kh is the largest of 8, 4, 2, 1 dividing the heads per
-    // group, and y / z extents are limited to 65535, so longer batches go in
-    // several launches of up to 65535 sequences
+  if (p.disable || varlen) {
+    // head-run kernels (no-write, or packed chains that write state): grid
+    // (row tiles, runs of kh heads of one group, sequences); y / z extents
+    // are limited to 65535, so longer batches go in several launches of up
+    // to 65535 sequences
     using NT = NoWriteTune<ST, N>;
-    const int kh = p.hr % 8 == 0 ? 8 : p.hr % 4 == 0 ? 4 : p.hr % 2 == 0 ? 2 : 1;
     p.tiles = (p.P + NT::ROWS - 1) / NT::ROWS;
     set_divisors(p);
+    const int kh = heads_per_cta(p.hr, nitems * p.H * (int64_t)p.tiles);
     if (p.H / kh > 65535) return cudaErrorInvalidConfiguration;
-    auto kern = varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
-                       : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
-    // several CTAs of up to 45 KB static shared memory per SM: ask for the
-    // largest shared-memory carveout
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
     const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
     const VarlenArgs v0 = va ? *va : VarlenArgs{};
     constexpr int64_t kZ = 65535;
+    if (p.disable) {
+      auto kern = varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
+                         : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
+      // several CTAs of up to 45 KB static shared memory per SM: ask for the
+      // largest shared-memory carveout
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           (int)cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+      for (int64_t s0 = 0; s0 < nitems; s0 += kZ) {
+        const dim3 grid((unsigned)p.tiles, (unsigned)(p.H / kh),
+                        (unsigned)std::min(kZ, nitems - s0));
+        kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, s0, kh);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+      }
+      return cudaSuccess;
+    }
+    auto kern = ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     for (int64_t s0 = 0; s0 < nitems; s0 += kZ) {
-      const dim3 grid((unsigned)p.tiles, (unsigned)(p.H / kh), (unsigned)std::min(kZ, nitems - s0));
-      kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, s0, kh);
+      const dim3 grid((unsigned)p.tiles, (unsigned)(p.H / kh),
+                      (unsigned)std::min(kZ, nitems - s0));
+      kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, v0, s0, kh);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
@@ -200,13 +224,8 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
   set_divisors(p);
   const int64_t grid = nitems * (int64_t)p.H * p.tiles;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if (varlen) {
-    ssu_varlen_kernel<ST, IT, N, T::WARPS, T::UNR, T::LMAX>
-        <<<(unsigned)grid, Cfg::THREADS, 0, stream>>>(p, *va);
-  } else {
-    ssu_one_token_kernel<ST, IT, N, T::WARPS, T::UNR>
-        <<<(unsigned)grid, Cfg::THREADS, 0, stream>>>(p, *oa);
-  }
+  ssu_one_token_kernel<ST, IT, N, T::WARPS, T::UNR>
+      <<<(unsigned)grid, Cfg::THREADS, 0, stream>>>(p, *oa);
   return cudaGetLastError();
 }
 
