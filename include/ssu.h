@@ -67,13 +67,10 @@ typedef enum ssu_status {
  *   SSU_ALGO_AUTO    the library's choice, the faster as measured: BULK for
  *                    ssu_update, DIRECT for ssu_update_varlen and for every
  *                    call with disable_state_update
- *   SSU_ALGO_DIRECT  ssu_update: one CTA per (sequence, head, 64-row tile);
- *                    each thread loads its state chunks straight into
- *                    registers.  ssu_update_varlen, and every call with
- *                    disable_state_update: one CTA per (sequence, run of
- *                    heads of one group, row tile), state tiles copied
- *                    asynchronously into shared memory while the previous
- *                    head computes.  With disable_state_update the steps of
+ *   SSU_ALGO_DIRECT  one CTA per (sequence, run of heads of one group, row
+ *                    tile); slot lookups and B / C staged once for the run,
+ *                    each head's state tile copied asynchronously into
+ *                    shared memory while the previous head computes.  With disable_state_update the steps of
  *                    a chain are taken in closed form (no state is stored,
  *                    so y_t needs only C_t . h, C_t . B_s and products of
  *                    dA); C_t . h on tensor cores (exact 16-bit products,

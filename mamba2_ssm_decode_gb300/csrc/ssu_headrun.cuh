@@ -739,9 +739,10 @@ struct StageView {
 // computes); each head then runs exactly the steps of the register kernel
 // (step_rows, the same staged values and stores, so the same bits).  Chains
 // longer than LMAX take the register kernel's block, head by head.
-template <class ST, class IT, int N, int WARPS, int UNR, int LMAX>
+template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, bool VARLEN>
 __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
-    ssu_run_kernel(const KParams p, const VarlenArgs va, int64_t seq0, int kh) {
+    ssu_run_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t seq0,
+                   int kh) {
   using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
   using L = typename Cfg::L;
   constexpr int ROWS = Cfg::ROWS;
@@ -761,15 +762,27 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
   int64_t r0, src;
   int len;
   bool read_ok;
-  if (!varlen_item(p, va, s, &r0, &len, &src, &read_ok)) return;
+  if constexpr (VARLEN) {
+    if (!varlen_item(p, va, s, &r0, &len, &src, &read_ok)) return;
+  } else {
+    r0 = s;
+    len = 1;
+    src = oa.sbi ? load_int(oa.sbi, s, oa.idx64) : s;
+    read_ok = slot_ok(src, p.pad, p.slots);
+  }
   const TableArgs dtab = va.dst.idx ? va.dst : va.src;  // no write table: the read table
-  const int idx64 = va.idx64;
-  auto dst_of = [dtab, idx64, s](int t, int64_t* o) -> bool {
-    if (dtab.idx) return table_entry(dtab, s, t, idx64, o);
-    *o = s;
+  const int idx64 = VARLEN ? va.idx64 : oa.idx64;
+  const void* dsbi = oa.dsbi;
+  auto dst_of = [dtab, idx64, s, dsbi, src](int t, int64_t* o) -> bool {
+    if constexpr (VARLEN) {
+      if (dtab.idx) return table_entry(dtab, s, t, idx64, o);
+      *o = s;
+    } else {
+      *o = dsbi ? load_int(dsbi, s, idx64) : src;
+    }
     return true;
   };
-  if (len > LMAX) {
+  if (VARLEN && len > LMAX) {
     StageT& stg = *reinterpret_cast<StageT*>(raw);
     for (int k = 0; k < kh; ++k) {
       ssu_block_on<ST, IT, N, WARPS, UNR, LMAX>(stg, p, h0 + k, p0, r0, len, src, read_ok,

@@ -542,28 +542,4 @@ __device__ __forceinline__ bool varlen_item(const KParams& p, const VarlenArgs& 
   return true;
 }
 
-template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, class DstFn>
-__device__ __forceinline__ void ssu_block(const KParams& p, int h, int p0, int64_t r0, int len,
-                                          int64_t src, bool read_ok, DstFn dst_of) {
-  __shared__ Stage<N, SSUConfig<ST, IT, N, WARPS, UNR, LMAX>::ROWS, LMAX> stg;
-  ssu_block_on<ST, IT, N, WARPS, UNR, LMAX>(stg, p, h, p0, r0, len, src, read_ok, dst_of);
-}
-
-// One-token decode: blockIdx -> (sequence b, head, row tile).
-template <class ST, class IT, int N, int WARPS, int UNR>
-__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
-    ssu_one_token_kernel(const KParams p, const OneTokenArgs a) {
-  int64_t b;
-  int h, tile;
-  split_index(p, blockIdx.x, &b, &h, &tile);
-  using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, 1>;
-  const int p0 = tile * Cfg::ROWS;
-
-  const int64_t src = a.sbi ? load_int(a.sbi, b, a.idx64) : b;
-  const bool read_ok = slot_ok(src, p.pad, p.slots);
-  const int64_t dst = a.dsbi ? load_int(a.dsbi, b, a.idx64) : src;
-  ssu_block<ST, IT, N, WARPS, UNR, 1>(p, h, p0, b, 1, src, read_ok,
-                                      [dst](int, int64_t* o) { *o = dst; return true; });
-}
-
 }  // namespace ssu

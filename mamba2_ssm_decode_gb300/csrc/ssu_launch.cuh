@@ -32,9 +32,9 @@ struct Tune {
   static constexpr int LMAX = 4;
 };
 
-// No-write kernel: state tiles of at most 16 KB, two per CTA.
+// Head-run kernels: state tiles of at most 16 KB, two per CTA.
 template <class ST, int N>
-struct NoWriteTune {
+struct HeadRunTune {
   using L = RowLayout<ST, N>;
   static constexpr int WARPS = 4;
   static constexpr int UNR = cmax(
@@ -164,10 +164,8 @@ template <class ST, class IT, int N>
 cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const VarlenArgs* va,
                          int64_t nitems, cudaStream_t stream, int algorithm) {
   using T = Tune<ST, N>;
-  using Cfg = SSUConfig<ST, IT, N, T::WARPS, T::UNR, T::LMAX>;
   // auto (the fastest as measured): the bulk-copy pipeline for one-token calls
-  // that write state, the register kernel for multi-token chains that do, the
-  // no-write kernel for every call that writes none
+  // that write state, the head-run kernels for every other call
   const bool auto_bulk = !varlen && !p.disable;
   const bool bulk = algorithm == 2 /* SSU_ALGO_BULK */ || (algorithm == 0 && auto_bulk);
   if (bulk) {
@@ -177,56 +175,48 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
                   : launch_bulk<ST, IT, N, false>(p, o0, v0, nitems, stream);
   }
   if (nitems <= 0) return cudaSuccess;
-  if (p.disable || varlen) {
-    // head-run kernels (no-write, or packed chains that write state): grid
-    // (row tiles, runs of kh heads of one group, sequences); y / z extents
-    // are limited to 65535, so longer batches go in several launches of up
-    // to 65535 sequences
-    using NT = NoWriteTune<ST, N>;
-    p.tiles = (p.P + NT::ROWS - 1) / NT::ROWS;
-    set_divisors(p);
-    const int kh = heads_per_cta(p.hr, nitems * p.H * (int64_t)p.tiles);
-    if (p.H / kh > 65535) return cudaErrorInvalidConfiguration;
-    const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
-    const VarlenArgs v0 = va ? *va : VarlenArgs{};
-    constexpr int64_t kZ = 65535;
-    if (p.disable) {
-      auto kern = varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
-                         : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
-      // several CTAs of up to 45 KB static shared memory per SM: ask for the
-      // largest shared-memory carveout
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                           (int)cudaSharedmemCarveoutMaxShared);
-      if (e != cudaSuccess) return e;
-      for (int64_t s0 = 0; s0 < nitems; s0 += kZ) {
-        const dim3 grid((unsigned)p.tiles, (unsigned)(p.H / kh),
-                        (unsigned)std::min(kZ, nitems - s0));
-        kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, s0, kh);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-      }
-      return cudaSuccess;
-    }
-    auto kern = ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX>;
+  // head-run kernels: grid (row tiles, runs of kh heads of one group,
+  // sequences); y / z extents are limited to 65535, so longer batches go in
+  // several launches of up to 65535 sequences
+  using NT = HeadRunTune<ST, N>;
+  p.tiles = (p.P + NT::ROWS - 1) / NT::ROWS;
+  set_divisors(p);
+  const int kh = heads_per_cta(p.hr, nitems * p.H * (int64_t)p.tiles);
+  if (p.H / kh > 65535) return cudaErrorInvalidConfiguration;
+  const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
+  const VarlenArgs v0 = va ? *va : VarlenArgs{};
+  constexpr int64_t kZ = 65535;
+  if (p.disable) {
+    auto kern = varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
+                       : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
+    // several CTAs of up to 45 KB static shared memory per SM: ask for the
+    // largest shared-memory carveout
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     for (int64_t s0 = 0; s0 < nitems; s0 += kZ) {
       const dim3 grid((unsigned)p.tiles, (unsigned)(p.H / kh),
                       (unsigned)std::min(kZ, nitems - s0));
-      kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, v0, s0, kh);
+      kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, s0, kh);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
   }
-  p.tiles = (p.P + Cfg::ROWS - 1) / Cfg::ROWS;
-  set_divisors(p);
-  const int64_t grid = nitems * (int64_t)p.H * p.tiles;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  ssu_one_token_kernel<ST, IT, N, T::WARPS, T::UNR>
-      <<<(unsigned)grid, Cfg::THREADS, 0, stream>>>(p, *oa);
-  return cudaGetLastError();
+  auto kern = varlen ? ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
+                     : ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
+  // up to 45 KB of static shared memory per CTA: the largest carveout
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  for (int64_t s0 = 0; s0 < nitems; s0 += kZ) {
+    const dim3 grid((unsigned)p.tiles, (unsigned)(p.H / kh),
+                    (unsigned)std::min(kZ, nitems - s0));
+    kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, s0, kh);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 template <class ST, class IT>
