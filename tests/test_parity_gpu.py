@@ -479,3 +479,26 @@ def test_workload_sweep_sampled(oracle_mod, b, sdt, mode, disable):
     assert res["rows"] >= len(seqs)
     del case
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# more sequences than one launch of the head-run kernels holds
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("disable", [False, True])
+@pytest.mark.parametrize("kind", ["single", "varlen"])
+def test_more_sequences_than_one_launch(oracle_mod, kind, disable):
+    """The head-run kernels put sequences on the grid's z extent (at most 65535)
+    and split longer batches into several launches: every element on both sides
+    of the 65535-sequence boundary matches the oracle."""
+    kw = dict(heads=1, headdim=16, dstate=16, groups=1, state_dtype=torch.float32,
+              pad_frac=0.01, disable_state_update=disable, device=DEV)
+    if kind == "single":
+        case = W.single_token_case(batch=70001, slots=70010, seed=71, **kw)
+    else:
+        case = W.varlen_case(nseqs=66000, max_len=2, slots=132010, same_tables=True, seed=72,
+                             **kw)
+    r = P.parity(oracle_mod, case, label=f"{kind} disable={disable} beyond one launch",
+                 algorithm="direct")
+    if not disable:
+        assert r["slots_written"] > 65535
