@@ -802,7 +802,8 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     dsts[i] = v;
   }
 
-  // 1. state tiles of the first two heads by 16-byte async copies
+  // 1. the first head's state tile by 16-byte async copies (each head's tile
+  //    is issued one head ahead)
   const int64_t block_elems = (int64_t)p.P * N;
   const int nrows = p.P - p0 < ROWS ? p.P - p0 : ROWS;
   const int valid = read_ok ? nrows * N * (int)sizeof(ST) / 16 : 0;
@@ -823,7 +824,6 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     cp_async_commit();
   };
   issue_tile(0, 0);
-  issue_tile(1, 1);
 
   // 2. B / C, the per-head dt' / dA table and the first head's rows
   const bool tied = per_head_dt(p);
@@ -842,8 +842,10 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
   const int jbase = warp * UNR * L::RPW + rr;
   ST* state = static_cast<ST*>(p.state);
   for (int k = 0; k < kh; ++k) {
-    cp_async_wait<1>();  // head k's copies (the newest group is head k + 1's)
-    __syncthreads();     // ... from every thread; hrows[k & 1] complete
+    cp_async_wait<0>();  // head k's copies
+    __syncthreads();     // ... from every thread; hrows[k & 1] complete; buffer
+                         // (k + 1) & 1 was read (head k - 1) before this point
+    issue_tile(k + 1, (k + 1) & 1);  // in flight during head k's steps
     const int h = h0 + k;
     // 3. this thread's state chunks of head k, widened to fp32
     float2 hs[UNR][L::EPL / 2];
@@ -859,8 +861,6 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
                             &hs[u][c * L::VEC / 2]);
       }
     }
-    __syncthreads();  // every thread has its chunks: the buffer goes to head k + 2
-    issue_tile(k + 2, k & 1);
     // 4. the next head's rows (into the other buffer)
     if (k + 1 < kh) {
       pre.load(p, h + 1, tied);
