@@ -15,8 +15,8 @@
 // the slots, arms full[s] with the tile's byte count and issues one bulk copy
 // of the tile's contiguous rows (or just arrives, for a pad / invalid read
 // slot).  The consumer warps wait full[s], read their chunks of the tile into
-// fp32 registers, release the stage at once, then run the steps exactly as the
-// register kernel does (same lane layout, same arithmetic, same stores).
+// fp32 registers, release the stage at once, then run the steps of step_rows
+// (the lane layout, arithmetic and stores of the head-run kernel).
 // Two kernels differ in who stages the item's per-step operands (B, C, dA,
 // dt' x, D x, silu z): in ssu_bulk_kernel the producer warp converts them into
 // a ring of operand buffers one item ahead; in ssu_bulk_cs_kernel the consumer

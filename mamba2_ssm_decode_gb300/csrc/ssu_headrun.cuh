@@ -2,9 +2,9 @@
 // group for one sequence (and one row tile), so the slot lookup, the B / C
 // staging and the per-head dt' / dA are done once for the run, and the state
 // tiles of the next heads (contiguous in the slot) land in shared memory by
-// cp.async while the current head computes.  Two kernels: packed chains that
-// write state (ssu_run_kernel, exactly the register kernel's steps per head),
-// and calls that write no state (ssu_nowrite_kernel, below).
+// cp.async while the current head computes.  Two kernels: calls that write
+// state (ssu_run_kernel, the step-by-step update of step_rows per head), and
+// calls that write no state (ssu_nowrite_kernel).
 //
 // Calls that write no state: the steps of a staged chunk have a closed form.
 // Unrolling h_t = dA_t h_{t-1} + dtx_t B_t from the chunk's initial state h:
@@ -732,13 +732,14 @@ struct StageView {
   const float (*gate)[ROWS];
 };
 
-// Packed chains that write state: grid (row tiles, runs of kh heads of one
-// group, sequences).  The slot lookups, the chain's write slots, B / C and
-// the per-head dt' / dA table are formed once for the run; each head's state
-// tile lands in shared memory by cp.async (the next two in flight while one
-// computes); each head then runs exactly the steps of the register kernel
-// (step_rows, the same staged values and stores, so the same bits).  Chains
-// longer than LMAX take the register kernel's block, head by head.
+// Calls that write state (packed chains, or one token): grid (row tiles, runs
+// of kh heads of one group, sequences).  The slot lookups, the chain's write
+// slots, B / C and the per-head dt' / dA table are formed once for the run;
+// each head's state tile lands in shared memory by cp.async, issued one head
+// ahead so it is in flight while the previous head computes; each head then
+// runs step_rows on the same staged values, with the same stores, as the bulk
+// kernels (so the same bits).  Chains longer than LMAX take the per-head block
+// (ssu_block_on), head by head.
 template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, bool VARLEN>
 __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     ssu_run_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t seq0,
