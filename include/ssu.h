@@ -28,8 +28,9 @@
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
  *     allocates nothing, never synchronises, never copies device data to the
- *     host, and issues at most one kernel launch on `stream` (a
- *     cudaStream_t; NULL is the legacy default stream).
+ *     host, and issues one kernel launch on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) -- one per 65535 sequences for a larger
+ *     batch on the DIRECT path, whose grid holds sequences in its z extent.
  *   - Arguments are validated on the host before any launch; a rejected call
  *     launches nothing and changes nothing.  SSU_ERR_INVALID_ARGUMENT mirrors
  *     the pages' ValueError cases, SSU_ERR_UNSUPPORTED their
