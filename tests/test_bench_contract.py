@@ -1,0 +1,74 @@
+"""bench.py's output line: the keys and units the measurement contract fixes.
+
+The reference arm (the CPU oracle on a bounded sample) runs without a GPU; the
+timed arm of the CUDA path needs one."""
+from __future__ import annotations
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_bench(*args, timeout=600):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                       capture_output=True, text=True, timeout=timeout)
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    return r, (json.loads(lines[-1]) if lines else None)
+
+
+def check_common(d, steps, warmup):
+    assert d["metric"] == "SSU decode tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+    assert d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == steps and d["warmup"] == warmup
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["scaling"] == "weak" and d["vs_baseline"] is None
+    assert d["data"].startswith("synthetic")
+    assert d["config"]["workload"] == "mamba2-2.7b-decode-b256"
+
+
+def test_reference_arm_line():
+    r, d = run_bench("--impl", "reference", "--steps", "3", "--warmup", "3")
+    assert r.returncode == 0, r.stderr[-2000:]
+    check_common(d, 3, 3)
+    assert d["impl"] == "reference" and d["dtype"] == "f64"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert cb["unit"] == "tokens/s" and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_too_few_warmup_steps_rejected():
+    r, d = run_bench("--steps", "3", "--warmup", "2", timeout=120)
+    assert r.returncode != 0 and d is None
+    assert "--warmup must be >= 3" in r.stderr
+
+
+@pytest.mark.gpu
+def test_cuda_arm_line():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mamba2_ssm_decode_gb300 import build
+    build.build()
+    r, d = run_bench("--steps", "20", "--warmup", "3", "--no-extras", "--cpu-seconds", "0.5")
+    assert r.returncode == 0, r.stderr[-2000:]
+    check_common(d, 20, 3)
+    assert d["dtype"] == "f32"
+    rf = d["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
+    assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
+    assert rf["traffic"] is None or rf["traffic"] > 0
+    e = d["e2e"]
+    assert e["unit"] == "tokens/s" and 0 < e["value"] <= d["value"] * 1.05
+    assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] == 20          # one SSU launch per timed step
+    ck = d["clocks"]
+    assert ck["sm_max_mhz"] > 0 and isinstance(ck["reasons"], list)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
