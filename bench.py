@@ -18,7 +18,7 @@ and, with extras on, the other serving workloads (`workloads`).
 Under torchrun (N > 1) every rank runs its own shard of sequences (its own
 seed) on its own GPU: weak scaling, no data-path collective; ranks meet only
 at the barriers around the timed region and the max-reduction of its time.
-`--impl reference` times the CPU oracle (the reference arm of this build) on
+`--impl reference` times the CPU oracle (the reference arm) on
 the same workload, on rank 0 only.
 """
 from __future__ import annotations

@@ -57,7 +57,7 @@ struct CUstream_st; /* cudaStream_t */
 typedef enum ssu_status {
   SSU_OK = 0,
   SSU_ERR_INVALID_ARGUMENT = 1, /* shapes, strides, dtypes or values the contract rejects */
-  SSU_ERR_UNSUPPORTED = 2,      /* a valid request this build does not implement */
+  SSU_ERR_UNSUPPORTED = 2,      /* a valid request the library does not implement */
   SSU_ERR_CUDA = 3              /* the kernel launch failed */
 } ssu_status;
 

@@ -6,7 +6,7 @@ current torch stream of the tensors' device.  Every step of the operation runs
 in libssu_gb300.so; there is no CPU or torch fallback.
 
 Exceptions follow the pages' conventions ("mate.mamba"): ValueError for a
-rejected argument, NotImplementedError for a capability this build does not
+rejected argument, NotImplementedError for a capability the library does not
 implement, RuntimeError for a failed launch.
 """
 from __future__ import annotations
