@@ -1,5 +1,5 @@
 """Plain fp64 CPU oracle for the Mamba2 selective state update and the ReplaySSM
-ring trackers.
+ring trackers (and, in ``oracle/ssd.py``, for the packed SSD prefill).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` may import this package; the product path never
