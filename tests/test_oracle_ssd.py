@@ -17,11 +17,19 @@ than itself:
 """
 from __future__ import annotations
 
+import importlib.util
+import os
+
 import numpy as np
 import pytest
 import torch
 
-from oracle import ssd
+if os.environ.get("SSD_ORACLE_PATH"):   # a planted-mistake copy (test_oracle_ssd_mutations.py)
+    _spec = importlib.util.spec_from_file_location("ssd_under_test", os.environ["SSD_ORACLE_PATH"])
+    ssd = importlib.util.module_from_spec(_spec)
+    _spec.loader.exec_module(ssd)
+else:
+    from oracle import ssd
 
 
 def chunks(lengths, chunk_size):
