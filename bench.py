@@ -293,6 +293,9 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+DATA = "synthetic (seeded random inputs of Mamba2 serving shapes)"
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mamba2_ssm_decode_gb300", "csrc")
@@ -515,7 +518,7 @@ def run_ours(args):
         "metric": "SSU decode tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random inputs of Mamba2 serving shapes)",
+        "vs_baseline": None, "dtype": "f32", "data": DATA,
         "config": {"workload": case.name, "batch": case.nseqs, "nheads": H, "headdim": P,
                    "dstate": N, "ngroups": G, "state_dtype": str(case.state.dtype)[6:],
                    "io_dtype": str(case.x.dtype)[6:], "slots": slots, "non_pad_tokens": tokens,
@@ -601,7 +604,7 @@ def run_reference(args):
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded random inputs of Mamba2 serving shapes)",
+        "data": DATA,
         "config": {"workload": case.name, "batch": case.nseqs, "nheads": H, "headdim": P,
                    "dstate": N, "ngroups": G, "state_dtype": str(case.state.dtype)[6:],
                    "non_pad_tokens": tokens_full, "parallelism": "rank 0 only"},
