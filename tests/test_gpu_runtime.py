@@ -1,5 +1,6 @@
 """GPU runtime properties of the library beyond parity: CUDA-graph capture of
-a decode step, and the bounded-wait failure path of the bulk-copy kernel."""
+decode steps on every kernel family, and the bounded-wait failure path of the
+bulk-copy kernel."""
 from __future__ import annotations
 
 import pytest
@@ -62,6 +63,53 @@ def test_decode_step_replays_in_a_cuda_graph(algo):
                                                       eager.prev_num_accepted),
                  (case.prev_query_len, eager.prev_query_len)):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("kind", ["one_token_direct", "no_write_mtp_bf16"])
+def test_head_run_calls_replay_in_a_cuda_graph(kind):
+    """A one-token call on the head-run kernel (DIRECT) and a no-write MTP call
+    (the tensor-core closed form) captured once and replayed three times give
+    the bits of the same calls made eagerly."""
+    import mamba2_ssm_decode_gb300 as ssu
+    if kind == "one_token_direct":
+        case = W.single_token_case(batch=96, heads=16, headdim=64, dstate=128, groups=2,
+                                   slots=96, state_dtype=torch.float32, identity_slots=True,
+                                   seed=21, device=DEV)
+
+        def step(c, o):
+            ssu.ssu_update(c.state, c.x, c.dt, c.A, c.B, c.C, D=c.D, z=c.z, dt_bias=c.dt_bias,
+                           dt_softplus=True, state_batch_indices=c.state_batch_indices, out=o,
+                           algorithm="direct")
+    else:
+        case = W.varlen_case(nseqs=64, max_len=4, heads=16, headdim=64, dstate=128, groups=2,
+                             slots=512, state_dtype=torch.bfloat16, disable_state_update=True,
+                             seed=22, device=DEV)
+
+        def step(c, o):
+            ssu.ssu_update_varlen(c.state, c.x, c.dt, c.A, c.B, c.C, D=c.D, z=c.z,
+                                  dt_bias=c.dt_bias, dt_softplus=True, cu_seqlens=c.cu_seqlens,
+                                  num_accepted_tokens=c.num_accepted_tokens,
+                                  state_batch_indices=c.state_batch_indices,
+                                  dst_state_batch_indices=c.dst_state_batch_indices,
+                                  disable_state_update=True, out=o)
+    eager = case.clone()
+    out = torch.empty_like(case.x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(case.clone(), torch.empty_like(out))   # set-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(case, out)
+    assert torch.equal(case.state, eager.state)
+    out_e = torch.empty_like(out)
+    for _ in range(3):
+        g.replay()
+        step(eager, out_e)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_e)
+    assert torch.equal(case.state, eager.state)
 
 
 def test_bounded_wait_gives_up_and_the_context_stays_usable(oracle_mod):
