@@ -163,44 +163,48 @@ class Step:
         else:
             self.v4 = None
 
-    def ssu_launch(self, x=None, z=None, dt=None, B=None, C=None, sbi=None, out=None):
+    # the tensors a caller supplies anew every step (everything but the state
+    # pool, the trackers and the per-head parameters)
+    STEP_INPUTS = ("x", "z", "dt", "B", "C", "state_batch_indices", "dst_state_batch_indices",
+                   "cu_seqlens", "num_accepted_tokens")
+
+    def ssu_launch(self, out=None, **over):
         c = self.case
-        x = c.x if x is None else x
-        z = c.z if z is None else z
-        dt = c.dt if dt is None else dt
-        B = c.B if B is None else B
-        C = c.C if C is None else C
-        sbi = c.state_batch_indices if sbi is None else sbi
+        t = {n: over[n] if over.get(n) is not None else getattr(c, n) for n in self.STEP_INPUTS}
         out = self.out if out is None else out
-        kw = dict(D=c.D, z=z, dt_bias=c.dt_bias, dt_softplus=c.dt_softplus,
+        kw = dict(D=c.D, z=t["z"], dt_bias=c.dt_bias, dt_softplus=c.dt_softplus,
                   pad_slot_id=c.pad_slot_id, disable_state_update=c.disable_state_update,
                   out=out, algorithm=self.algorithm)
         if c.kind == "single":
-            self.ssu.ssu_update(c.state, x, dt, c.A, B, C, state_batch_indices=sbi,
-                                dst_state_batch_indices=c.dst_state_batch_indices, **kw)
+            self.ssu.ssu_update(c.state, t["x"], t["dt"], c.A, t["B"], t["C"],
+                                state_batch_indices=t["state_batch_indices"],
+                                dst_state_batch_indices=t["dst_state_batch_indices"], **kw)
         elif self.v4 is not None:
             v = self.v4
-            kw["z"], kw["out"] = v(z), v(out)
-            self.ssu.ssu_update_varlen(c.state, v(x), v(dt), c.A, v(B), v(C),
-                                       num_accepted_tokens=c.num_accepted_tokens,
-                                       state_batch_indices=sbi,
-                                       dst_state_batch_indices=c.dst_state_batch_indices, **kw)
+            kw["z"], kw["out"] = v(t["z"]), v(out)
+            self.ssu.ssu_update_varlen(c.state, v(t["x"]), v(t["dt"]), c.A, v(t["B"]),
+                                       v(t["C"]), num_accepted_tokens=t["num_accepted_tokens"],
+                                       state_batch_indices=t["state_batch_indices"],
+                                       dst_state_batch_indices=t["dst_state_batch_indices"],
+                                       **kw)
         else:
-            self.ssu.ssu_update_varlen(c.state, x, dt, c.A, B, C, cu_seqlens=c.cu_seqlens,
-                                       num_accepted_tokens=c.num_accepted_tokens,
-                                       state_batch_indices=sbi,
-                                       dst_state_batch_indices=c.dst_state_batch_indices,
+            self.ssu.ssu_update_varlen(c.state, t["x"], t["dt"], c.A, t["B"], t["C"],
+                                       cu_seqlens=t["cu_seqlens"],
+                                       num_accepted_tokens=t["num_accepted_tokens"],
+                                       state_batch_indices=t["state_batch_indices"],
+                                       dst_state_batch_indices=t["dst_state_batch_indices"],
                                        nseqs=c.nseqs, **kw)
 
-    def trackers(self, sbi=None):
+    def trackers(self, **over):
         c = self.case
         if c.ring_start is None:
             return
-        sbi = c.state_batch_indices if sbi is None else sbi
+        t = {n: over[n] if over.get(n) is not None else getattr(c, n) for n in self.STEP_INPUTS}
+        sbi = t["state_batch_indices"]
         tr = (c.ring_start, c.prev_num_accepted, c.prev_query_len)
         self.ssu.ssu_ring_update(*tr, sbi, c.logical_window, c.ring_buffer_len,
                                  pad_slot_id=c.pad_slot_id)
-        self.ssu.ssu_ring_commit(*tr, sbi, c.num_accepted_tokens, c.cu_seqlens,
+        self.ssu.ssu_ring_commit(*tr, sbi, t["num_accepted_tokens"], t["cu_seqlens"],
                                  c.logical_window, c.ring_buffer_len, pad_slot_id=c.pad_slot_id)
 
     def __call__(self):
@@ -212,22 +216,83 @@ class Step:
 # clocks
 # ---------------------------------------------------------------------------
 
-class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons for this GPU."""
+_REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40),
+            ("sw_thermal_slowdown", 0x20), ("sw_power_cap", 0x4))
 
-    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+class _Nvml:
+    """SM clock and clock-event reasons of one GPU read through NVML (ctypes on
+    the driver's libnvidia-ml; read-only queries)."""
+
+    def __init__(self, uuid):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        n = ctypes.c_uint(0)
+        if lib.nvmlDeviceGetCount_v2(ctypes.byref(n)) != 0:
+            raise OSError("nvmlDeviceGetCount failed")
+        self.h = None
+        buf = ctypes.create_string_buffer(96)
+        for i in range(n.value):
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(i, ctypes.byref(h)) != 0:
+                continue
+            if lib.nvmlDeviceGetUUID(h, buf, 96) != 0:
+                continue
+            if buf.value.decode().lower().replace("gpu-", "") == uuid:
+                self.h = h
+                break
+        if self.h is None:
+            raise OSError("GPU not found by UUID")
+        self.lib = lib
+        try:
+            self._reasons = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))   # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+
+    def read(self):
+        ct = self.ct
+        sm = ct.c_uint(0)
+        r = ct.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(sm)) != 0:
+            return None
+        self._reasons(self.h, ct.byref(r))
+        return float(sm.value), self.max_mhz, frozenset(n for n, b in _REASONS if r.value & b)
+
+
+class ClockSampler:
+    """SM clock and throttle reasons of this GPU, sampled every millisecond
+    through NVML (so that even a few-millisecond timed region holds samples),
+    or every 100 ms from nvidia-smi where NVML cannot be loaded."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device):
         props = torch.cuda.get_device_properties(device)
         self.uuid = str(getattr(props, "uuid", "")).lower().replace("gpu-", "")
-        self.samples = []
+        self.samples = []      # (time, sm MHz, max MHz, reasons)
         self.proc = None
         self.thread = None
+        self.stop_flag = threading.Event()
         self.marks = {}
+        self.source = None
 
     def start(self):
+        try:
+            nv = _Nvml(self.uuid)
+            self.source = "nvml 1 ms"
+            self.thread = threading.Thread(target=self._poll, args=(nv,), daemon=True)
+            self.thread.start()
+            return
+        except (OSError, AttributeError):
+            pass
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -235,23 +300,38 @@ class ClockSampler:
         except OSError:
             self.proc = None
             return
+        self.source = "nvidia-smi 100 ms"
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
 
+    def _poll(self, nv):
+        while not self.stop_flag.is_set():
+            v = nv.read()
+            if v is not None:
+                self.samples.append((time.perf_counter(), *v))
+            time.sleep(0.001)
+
     def _read(self):
+        names = [n for n, _ in _REASONS]
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 7:
                 continue
             uuid = parts[0].lower().replace("gpu-", "")
             if self.uuid and uuid != self.uuid:
                 continue
-            self.samples.append((time.perf_counter(), parts[1:]))
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = frozenset(n for n, v in zip(names, parts[3:7]) if v == "Active")
+            self.samples.append((time.perf_counter(), sm, mx, reasons))
 
     def mark(self, name):
         self.marks[name] = time.perf_counter()
 
     def stop(self):
+        self.stop_flag.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -263,22 +343,15 @@ class ClockSampler:
 
     def summary(self):
         t0, t1 = self.marks.get("timed_start"), self.marks.get("timed_end")
-        inside = [s for t, s in self.samples if t0 is not None and t0 <= t <= t1]
-        pool = inside or [s for _, s in self.samples]
-
-        def num(v):
-            try:
-                return float(v)
-            except ValueError:
-                return None
-
-        sm = [num(s[0]) for s in pool if num(s[0]) is not None]
-        mx = [num(s[1]) for s in pool if num(s[1]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for s in pool for n, v in zip(names, s[4:8]) if v.strip() == "Active"})
+        inside = [x for x in self.samples if t0 is not None and t0 <= x[0] <= t1]
+        pool = inside or self.samples
+        sm = [x[1] for x in pool]
+        mx = [x[2] for x in pool]
+        reasons = sorted({r for x in pool for r in x[3]})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(pool), "samples_in_timed_region": len(inside)}
+                "samples": len(pool), "samples_in_timed_region": len(inside),
+                "source": self.source}
 
 
 # ---------------------------------------------------------------------------
@@ -345,11 +418,13 @@ def time_steps(step, steps, stream, per_launch=True):
 
 def e2e(step, steps, warmup, stream):
     """The same step through the public API with host buffers: every step copies
-    its inputs (x, z, dt, B, C, slot table) from pinned host memory, runs the
-    call and copies y back, then waits for it."""
+    every per-step input (x, z, dt, B, C, the slot tables, cu_seqlens and the
+    acceptance counts) from pinned host memory, runs the call (and the tracker
+    update / commit where the workload has them) and copies y back, then waits
+    for it."""
     c = step.case
-    names = ["x", "z", "dt", "B", "C", "state_batch_indices"]
-    host = {n: getattr(c, n).cpu().pin_memory() for n in names if getattr(c, n) is not None}
+    host = {n: getattr(c, n).cpu().pin_memory() for n in step.STEP_INPUTS
+            if getattr(c, n) is not None}
     dev = {n: torch.empty_like(getattr(c, n)) for n in host}
     y_host = torch.empty(c.x.shape, dtype=c.x.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -359,9 +434,8 @@ def e2e(step, steps, warmup, stream):
         with torch.cuda.stream(stream):
             for n, t in host.items():
                 dev[n].copy_(t, non_blocking=True)
-            step.ssu_launch(x=dev["x"], z=dev.get("z"), dt=dev["dt"], B=dev["B"], C=dev["C"],
-                            sbi=dev.get("state_batch_indices"))
-            step.trackers(sbi=dev.get("state_batch_indices"))
+            step.ssu_launch(**dev)
+            step.trackers(**dev)
             y_host.copy_(step.out, non_blocking=True)
         stream.synchronize()
 
@@ -373,35 +447,106 @@ def e2e(step, steps, warmup, stream):
     return (time.perf_counter() - t0) * 1e3 / steps, h2d, d2h
 
 
-def cpu_baseline(case, min_seconds=10.0):
-    """The oracle (plain fp64 C, one thread) on host copies of the workload,
-    repeated until about `min_seconds` of CPU work."""
+STATE_TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-2, torch.float16: 2e-2}
+HALF_ULP = {torch.bfloat16: 2.0**-8, torch.float16: 2.0**-11, torch.float32: 0.0}
+
+
+def _excess(got, ref, tol, half_ulp=0.0):
+    """max |got - ref| / (tol + (tol + half_ulp) |ref|) (1.0 = at the tolerance)."""
+    got, ref = got.double(), ref.double()
+    if got.numel() == 0:
+        return 0.0
+    return float(((got - ref).abs() / (tol + (tol + half_ulp) * ref.abs())).max())
+
+
+def _oracle_call(sub):
     import oracle
-    cpu = case.to("cpu")
-    tokens, _, _ = accounting(cpu)
-    reps = 0
-    t0 = time.perf_counter()
-    while True:
-        state = cpu.state.clone()
-        kw = dict(D=cpu.D, z=cpu.z, dt_bias=cpu.dt_bias, dt_softplus=cpu.dt_softplus,
-                  pad_slot_id=cpu.pad_slot_id, disable_state_update=cpu.disable_state_update,
-                  state_batch_indices=cpu.state_batch_indices,
-                  dst_state_batch_indices=cpu.dst_state_batch_indices)
-        t = time.perf_counter()
-        if cpu.kind == "single":
-            oracle.ssu_update(state, cpu.x, cpu.dt, cpu.A, cpu.B, cpu.C, **kw)
-        else:
-            oracle.ssu_update_varlen(state, cpu.x, cpu.dt, cpu.A, cpu.B, cpu.C,
-                                     cu_seqlens=cpu.cu_seqlens, nseqs=cpu.nseqs,
-                                     dense_steps=cpu.dense_steps,
-                                     num_accepted_tokens=cpu.num_accepted_tokens, **kw)
-        reps += 1
-        if time.perf_counter() - t0 >= min_seconds:
-            break
-    secs = time.perf_counter() - t0
-    return {"value": tokens * reps / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"the whole {case.name} batch ({tokens} tokens), {reps} repetitions, "
-                      f"{secs:.1f} s on one host core (fp64 C oracle)"}
+    kw = dict(D=sub.D, z=sub.z, dt_bias=sub.dt_bias, dt_softplus=sub.dt_softplus,
+              pad_slot_id=sub.pad_slot_id, disable_state_update=sub.disable_state_update,
+              state_batch_indices=sub.state_batch_indices,
+              dst_state_batch_indices=sub.dst_state_batch_indices)
+    if sub.kind == "single":
+        return oracle.ssu_update(sub.state, sub.x, sub.dt, sub.A, sub.B, sub.C, **kw)
+    return oracle.ssu_update_varlen(sub.state, sub.x, sub.dt, sub.A, sub.B, sub.C,
+                                    cu_seqlens=sub.cu_seqlens, nseqs=sub.nseqs,
+                                    dense_steps=sub.dense_steps,
+                                    num_accepted_tokens=sub.num_accepted_tokens, **kw)
+
+
+def _time_oracle(shards, threads, min_seconds, passes=None):
+    """Oracle time per pass over `shards` (CPU sub-cases, disjoint slots) on
+    `threads` host threads (the oracle is C called through ctypes, which runs
+    with the interpreter lock released), repeated until `min_seconds` (or
+    exactly `passes` times).  Each shard runs on its own copy of its pool, made
+    before the clock starts; later passes continue from the state the previous
+    pass left (the time does not depend on the values).  Returns (seconds per
+    pass, passes, first pass's (y, pool) per shard)."""
+    import concurrent.futures as cf
+    import dataclasses
+    work = [dataclasses.replace(sub, state=sub.state.clone()) for sub in shards]
+    first = None
+    reps, t0 = 0, time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        while True:
+            ys = list(ex.map(_oracle_call, work))
+            if first is None:   # keep the first pass's results (not timed)
+                tc = time.perf_counter()
+                first = [(y, w.state.clone()) for y, w in zip(ys, work)]
+                t0 += time.perf_counter() - tc
+            reps += 1
+            if passes is not None:
+                if reps >= passes:
+                    break
+            elif time.perf_counter() - t0 >= min_seconds:
+                break
+    return (time.perf_counter() - t0) / reps, reps, first
+
+
+def cpu_leg(step, max_seqs, min_seconds):
+    """The CPU oracle (plain fp64 C) beside the GPU, on a bounded sample of the
+    workload: the first `max_seqs` sequences.  Their slots are copied to the host,
+    the GPU runs one more step of the whole batch, and the oracle runs the sample
+    once on one host thread and once on all host cores (the sample split into
+    contiguous shards, one per thread); both are timed.  The GPU step's outputs
+    and written slots of the sample are compared with the oracle's at the
+    stated tolerances."""
+    from mamba2_ssm_decode_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    case = step.case
+    seqs = list(range(min(max_seqs, case.nseqs)))
+    sub, rows, remap = W.subset_case(case, seqs)
+    tokens, _, _ = accounting(sub)
+    # the GPU step whose sample is checked
+    torch.cuda.synchronize()
+    step.ssu_launch()
+    torch.cuda.synchronize()
+    y_gpu = step.out[torch.tensor(rows, dtype=torch.long, device=step.out.device)].cpu()
+    old = list(remap.keys())
+    pool_gpu = (case.state[torch.tensor(old, dtype=torch.long, device=case.state.device)].cpu()
+                if old else None)
+    # one thread over the whole sample, then all cores over contiguous shards
+    t1, reps1, res1 = _time_oracle([sub], 1, min_seconds / 2)
+    ncores = max(1, min(os.cpu_count() or 1, len(seqs)))
+    bounds = [len(seqs) * k // ncores for k in range(ncores + 1)]
+    shards = [W.subset_case(sub, list(range(bounds[k], bounds[k + 1])))[0]
+              for k in range(ncores) if bounds[k + 1] > bounds[k]]
+    tn, repsn, _ = _time_oracle(shards, len(shards), min_seconds / 2)
+    # parity of the GPU step on the sample
+    y_ref, st_ref = res1[0]
+    sdt = case.state.dtype
+    tol = STATE_TOL[sdt]
+    covered = ~torch.isnan(y_ref.reshape(y_ref.shape[0], -1)).any(dim=1)
+    y_err = _excess(y_gpu[covered].float(), y_ref[covered], tol, HALF_ULP[y_gpu.dtype])
+    st_err = _excess(pool_gpu.float(), st_ref.float(), tol) if pool_gpu is not None else 0.0
+    return {"value": tokens / tn, "unit": "tokens/s", "cores": len(shards), "kind": "oracle",
+            "single_core_value": tokens / t1,
+            "sample": f"the first {len(seqs)} of the {case.nseqs} sequences of {case.name} "
+                      f"({tokens} tokens): {reps1} pass(es) on one host core, {repsn} on "
+                      f"{len(shards)} threads (contiguous shards), fp64 C oracle",
+            "parity": {"sequences": len(seqs), "rows": len(rows),
+                       "y_err_over_tol": y_err, "state_err_over_tol": st_err,
+                       "ok": bool(y_err <= 1.0 and st_err <= 1.0)}}
 
 
 def measure(name, device, seed, steps, warmup, stream, algorithm="auto"):
@@ -425,12 +570,15 @@ def measure(name, device, seed, steps, warmup, stream, algorithm="auto"):
 
 DEFAULT_WORKLOAD = "mamba2-2.7b-decode"
 EXTRAS = ["hybrid-grouped-decode", "mtp-varlen",
+          "mamba2-2.7b-decode-perchannel", "mtp-varlen-dtperdim",
           "sweep-single-float32-b1024", "sweep-single-bfloat16-b1024",
           "sweep-mtp-float32-b1024", "sweep-mtp-bfloat16-b1024",
-          "sweep-single-float32-b4096", "sweep-single-bfloat16-b4096",
-          "sweep-mtp-float32-b4096", "sweep-mtp-bfloat16-b4096",
+          "sweep-single-bfloat16-b4096", "sweep-mtp-bfloat16-b4096",
           "sweep-single-float32-b1024-nowrite", "sweep-single-bfloat16-b1024-nowrite",
           "sweep-mtp-float32-b1024-nowrite", "sweep-mtp-bfloat16-b1024-nowrite"]
+# the largest single-GPU points, measured like the headline (every timed step,
+# end to end, oracle baseline and parity sample)
+LARGE = ["sweep-single-float32-b4096", "sweep-mtp-float32-b4096"]
 
 
 def dist_setup(n_gpus):
@@ -470,18 +618,13 @@ def sum_over_ranks(v, world, device):
     return float(t.item())
 
 
-def run_ours(args):
-    from mamba2_ssm_decode_gb300 import build as _b
-    world, rank, local = dist_setup(args.gpus)
-    if rank == 0 or world == 1:
-        _b.build()
-    barrier(world)
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    stream = torch.cuda.Stream(device)
+def headline(name, args, world, device, stream, peak, peak_kind, cpu=True):
+    """Every measurement of one workload: the timed steps (barrier, max over
+    ranks), the SSU launch's roofline, the device error word, the end-to-end
+    rate through the public API and, on rank 0, the oracle leg."""
+    rank = int(os.environ.get("RANK", "0"))
     seed = args.seed + rank   # each rank: its own shard of sequences
-
-    case = _workload(args.workload, device, seed)
+    case = _workload(name, device, seed)
     tokens, ssu_bytes, _ = accounting(case)
     step = Step(case, args.algorithm)
     with torch.cuda.stream(stream):
@@ -500,45 +643,73 @@ def run_ours(args):
     barrier(world)
     time.sleep(0.15)
     clocks.stop()
+    device_error = step.ssu.ssu_device_error()
     total_max = max_over_ranks(total, world, device)
     launch_max = max_over_ranks(launch, world, device)
     tokens_all = sum_over_ranks(tokens * args.steps, world, device)
     ms = total_max / args.steps
-    value = tokens_all / (total_max * 1e-3)
-
-    # end to end through the public API with host buffers
     e2e_ms, h2d, d2h = e2e(step, max(3, min(args.steps, 200)), 3, stream)
     e2e_ms = max_over_ranks(e2e_ms, world, device)
     e2e_value = sum_over_ranks(tokens, world, device) / (e2e_ms * 1e-3)
-
-    peak, peak_kind = measured_peak()
     achieved = ssu_bytes / (launch_max * 1e-3) / 1e9
     slots, H, P, N, G = case.dims
-    line = {
-        "metric": "SSU decode tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)",
-        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": DATA,
+    out = {
+        "value": tokens_all / (total_max * 1e-3), "ms_per_step": ms,
         "config": {"workload": case.name, "batch": case.nseqs, "nheads": H, "headdim": P,
                    "dstate": N, "ngroups": G, "state_dtype": str(case.state.dtype)[6:],
                    "io_dtype": str(case.x.dtype)[6:], "slots": slots, "non_pad_tokens": tokens,
+                   "rows": case.rows, "kind": case.kind,
+                   "disable_state_update": case.disable_state_update,
                    "algorithm": args.algorithm,
                    "l2": f"no flush: each step touches {ssu_bytes / 1e9:.2f} GB > 129 MB L2",
                    "parallelism": f"replicas x{world} (weak; independent sequence shards)"},
-        "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": ncu_traffic(args.workload),
+                     "frac": achieved / peak, "traffic": ncu_traffic(name),
                      "algorithmic_bytes_per_launch": ssu_bytes,
                      "launch_ms": launch_max, "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": step.launches * args.steps,
+        "device_error": device_error,
         "clocks": clocks.summary(),
     }
+    if device_error:
+        raise SystemExit(f"{case.name}: the device error word is {device_error:#x} after the "
+                         "timed steps (a bounded wait gave up)")
+    if cpu and rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_leg(step, 256 if name == DEFAULT_WORKLOAD else 48,
+                                      args.cpu_seconds if name == DEFAULT_WORKLOAD
+                                      else args.cpu_seconds / 2)
+    del step, case
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    from mamba2_ssm_decode_gb300 import build as _b
+    world, rank, local = dist_setup(args.gpus)
+    if rank == 0 or world == 1:
+        _b.build()
+    barrier(world)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    peak, peak_kind = measured_peak()
+
+    h = headline(args.workload, args, world, device, stream, peak, peak_kind)
+    line = {
+        "metric": "SSU decode tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)",
+        "value": h["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": h["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": DATA,
+        "config": h["config"], "hbm_gbs": h["roofline"]["achieved"],
+        "roofline": h["roofline"], "e2e": h["e2e"], "gpu_launches": h["gpu_launches"],
+        "device_error": h["device_error"], "clocks": h["clocks"],
+    }
+    if "cpu_baseline" in h:
+        line["cpu_baseline"] = h["cpu_baseline"]
     if not args.no_extras and world == 1:
         line["workloads"] = {}
-        del case, step
-        torch.cuda.empty_cache()
         for name in EXTRAS:
             c2, s2, r = measure(name, device, args.seed, max(5, min(args.steps, 50)), 3, stream,
                                 args.algorithm)
@@ -547,9 +718,14 @@ def run_ours(args):
                                                              "launch_ms", "ms_per_step")}
             del c2, s2
             torch.cuda.empty_cache()
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(_workload(args.workload, "cpu", args.seed),
-                                            min_seconds=args.cpu_seconds)
+        line["large_batch"] = {}
+        for name in LARGE:
+            r = headline(name, args, world, device, stream, peak, peak_kind)
+            line["large_batch"][r["config"]["workload"]] = r
+        line["device_error_after_extras"] = step_error = \
+            __import__("mamba2_ssm_decode_gb300").ssu_device_error()
+        if step_error:
+            raise SystemExit(f"device error word {step_error:#x} after the extra workloads")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -558,46 +734,32 @@ def run_ours(args):
 
 
 def run_reference(args):
-    """The reference arm: the CPU oracle on the same workload, rank 0 only."""
+    """The reference arm: the CPU oracle on the same workload, rank 0 only; each
+    step runs a bounded sample (the first 32 sequences) on all host cores."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import oracle
+    from mamba2_ssm_decode_gb300 import workloads as W
     oracle.build()
     case = _workload(args.workload, "cpu", args.seed)
     tokens_full, _, _ = accounting(case)
-    # each step: the oracle on a 32-sequence sample of the batch
-    from mamba2_ssm_decode_gb300 import workloads as W  # noqa: F401
     nsample = min(32, case.nseqs)
-    sample = _sample_sequences(case, nsample)
+    sample, _, _ = W.subset_case(case, list(range(nsample)))
     toks, _, _ = accounting(sample)
-
-    def one():
-        st = sample.state.clone()
-        kw = dict(D=sample.D, z=sample.z, dt_bias=sample.dt_bias, dt_softplus=sample.dt_softplus,
-                  pad_slot_id=sample.pad_slot_id,
-                  disable_state_update=sample.disable_state_update,
-                  state_batch_indices=sample.state_batch_indices,
-                  dst_state_batch_indices=sample.dst_state_batch_indices)
-        if sample.kind == "single":
-            oracle.ssu_update(st, sample.x, sample.dt, sample.A, sample.B, sample.C, **kw)
-        else:
-            oracle.ssu_update_varlen(st, sample.x, sample.dt, sample.A, sample.B, sample.C,
-                                     cu_seqlens=sample.cu_seqlens, nseqs=sample.nseqs,
-                                     dense_steps=sample.dense_steps,
-                                     num_accepted_tokens=sample.num_accepted_tokens, **kw)
-
-    for _ in range(args.warmup):
-        one()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        one()
-    secs = time.perf_counter() - t0
+    ncores = max(1, min(os.cpu_count() or 1, nsample))
+    bounds = [nsample * k // ncores for k in range(ncores + 1)]
+    shards = [W.subset_case(sample, list(range(bounds[k], bounds[k + 1])))[0]
+              for k in range(ncores) if bounds[k + 1] > bounds[k]]
+    _time_oracle(shards, len(shards), 0.0, passes=args.warmup)
+    per_pass, _, _ = _time_oracle(shards, len(shards), 0.0, passes=args.steps)
+    secs = per_pass * args.steps
     value = toks * args.steps / secs
     slots, H, P, N, G = case.dims
     sample_desc = (f"first {nsample} of the {case.nseqs} sequences of {case.name} "
-                   f"({toks} tokens) per step, fp64 C oracle, one host core")
+                   f"({toks} tokens) per step, fp64 C oracle on {len(shards)} host threads "
+                   f"(contiguous shards)")
     line = {
         "impl": "reference",
         "metric": "SSU decode tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)",
@@ -608,42 +770,12 @@ def run_reference(args):
         "config": {"workload": case.name, "batch": case.nseqs, "nheads": H, "headdim": P,
                    "dstate": N, "ngroups": G, "state_dtype": str(case.state.dtype)[6:],
                    "non_pad_tokens": tokens_full, "parallelism": "rank 0 only"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": sample_desc},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": len(shards),
+                         "kind": "oracle", "sample": sample_desc},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
-
-
-def _sample_sequences(case, n):
-    """The first n sequences of a CPU case, as a case of their own (same slots)."""
-    import dataclasses
-    if case.kind == "single":
-        rows = slice(0, n)
-        return dataclasses.replace(
-            case, x=case.x[rows], z=None if case.z is None else case.z[rows], dt=case.dt[rows],
-            B=case.B[rows], C=case.C[rows],
-            state_batch_indices=None if case.state_batch_indices is None
-            else case.state_batch_indices[:n],
-            dst_state_batch_indices=None if case.dst_state_batch_indices is None
-            else case.dst_state_batch_indices[:n], nseqs=n)
-    if case.cu_seqlens is not None:
-        end = int(case.cu_seqlens[n])
-        cu = case.cu_seqlens[: n + 1]
-    else:
-        end = n * case.dense_steps
-        cu = None
-    rows = slice(0, end)
-    return dataclasses.replace(
-        case, x=case.x[rows], z=None if case.z is None else case.z[rows], dt=case.dt[rows],
-        B=case.B[rows], C=case.C[rows], cu_seqlens=cu,
-        num_accepted_tokens=None if case.num_accepted_tokens is None
-        else case.num_accepted_tokens[:n],
-        state_batch_indices=None if case.state_batch_indices is None
-        else case.state_batch_indices[:n],
-        dst_state_batch_indices=None if case.dst_state_batch_indices is None
-        else case.dst_state_batch_indices[:n], nseqs=n)
 
 
 def main(argv=None):

@@ -27,10 +27,14 @@
  *
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
- *     allocates nothing, never synchronises, never copies device data to the
- *     host, and issues one kernel launch on `stream` (a cudaStream_t; NULL is
- *     the legacy default stream) -- one per 65535 sequences for a larger
- *     batch on the DIRECT path, whose grid holds sequences in its z extent.
+ *     allocates nothing and never copies device data to the host.  Each
+ *     compute or tracker call (ssu_update, ssu_update_varlen,
+ *     ssu_ring_update, ssu_ring_commit) issues exactly one kernel launch on
+ *     `stream` (a cudaStream_t; NULL is the legacy default stream), whatever
+ *     the batch, and never synchronises, so it can be captured in a CUDA
+ *     graph.  The two diagnostic calls (ssu_device_error,
+ *     ssu_selftest_bounded_wait) synchronise the device and must not be made
+ *     while any stream of the device is being captured.
  *   - Arguments are validated on the host before any launch; a rejected call
  *     launches nothing and changes nothing.  SSU_ERR_INVALID_ARGUMENT mirrors
  *     the pages' ValueError cases, SSU_ERR_UNSUPPORTED their
@@ -273,11 +277,19 @@ ssu_status ssu_ring_commit(int32_t* ring_start, int64_t ring_start_len,
                            int64_t pad_slot_id, struct CUstream_st* stream);
 
 /*
+ * Bits of the device-side error word (values, not bit positions).
+ */
+#define SSU_DEVICE_ERR_COPY_TIMEOUT 1u    /* a state tile copy never landed */
+#define SSU_DEVICE_ERR_RELEASE_TIMEOUT 2u /* a shared-memory stage was never released */
+
+/*
  * Device-side error word of the current device: nonzero after a kernel gave
- * up a bounded wait (bit 1: a tile copy never landed; bit 2: a stage was never
- * released).  No valid call sets it; it exists so that a fault in the copy
- * engine ends a kernel instead of hanging it.  This call SYNCHRONISES the
- * current device; reset != 0 clears the word afterwards.
+ * up a bounded wait (a mask of the SSU_DEVICE_ERR_* values above).  No valid
+ * call sets it; it exists so that a fault in the copy engine ends a kernel
+ * instead of hanging it.  There is one word per device, shared by every call
+ * and every host thread: a word set by one call stays set until it is reset.
+ * This call SYNCHRONISES the current device; reset != 0 clears the word
+ * afterwards.
  */
 ssu_status ssu_device_error(unsigned int* value, int reset);
 
@@ -285,9 +297,13 @@ ssu_status ssu_device_error(unsigned int* value, int reset);
  * Self-test of the bounded waits (no counterpart on the pages): launches, on
  * the current device's legacy default stream, one CTA that waits on an
  * mbarrier nothing completes; the wait must give up after limit_ns (0 <
- * limit_ns <= 1e9), set bit 1 of the device error word and return, leaving the
- * context usable.  *waited_ns receives the measured wait.  SYNCHRONISES the
- * device.
+ * limit_ns <= 1e9), set SSU_DEVICE_ERR_COPY_TIMEOUT in the device error word
+ * and return, leaving the context usable.  *waited_ns receives the measured
+ * wait.  SYNCHRONISES the device.  The measured wait is kept in one fixed
+ * device word shared by all calls, and the test sets the same error word as
+ * the compute kernels: self-tests that overlap each other, or compute calls
+ * in flight, race on those words, so run it alone and reset the error word
+ * afterwards (ssu_device_error(&v, 1)).
  */
 ssu_status ssu_selftest_bounded_wait(uint64_t limit_ns, uint64_t* waited_ns);
 

@@ -39,9 +39,11 @@ unsigned* device_error_word() {
 }
 
 int sm_count() {
+  static std::mutex mu;
   static int count[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lock(mu);
   if (count[dev] == 0) {
     int c = 0;
     cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);

@@ -29,6 +29,8 @@
 
 namespace ssu {
 
+// error word values (SSU_DEVICE_ERR_COPY_TIMEOUT / SSU_DEVICE_ERR_RELEASE_TIMEOUT
+// of the C ABI): a tile copy never landed / a stage was never released
 constexpr unsigned kErrFullTimeout = 1u;
 constexpr unsigned kErrEmptyTimeout = 2u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

@@ -485,12 +485,25 @@ __device__ __noinline__ void ssu_block_nowrite_chain(const KParams& p, int h, in
   }
 }
 
-// No-write kernel, one-token and packed routes: grid (row tiles, head runs
-// of kh heads of one group, sequences seq0 + z).  Sequences longer than
-// LMAX take the register form, head by head.
+// Coordinates of a head-run CTA: grid.x enumerates (run of kh heads, row
+// tile) with the tile fastest, grid.y x grid.z the sequences (z-major), so
+// consecutive CTAs stay on one slot's contiguous blocks and any batch fits
+// one launch.  False for the few CTAs past the last sequence.
+__device__ __forceinline__ bool head_run_coords(const KParams& p, int64_t nseqs, int kh,
+                                                int rows, int64_t* s, int* h0, int* p0) {
+  const uint32_t run = p.fd_tiles.div(blockIdx.x);
+  *p0 = (int)(blockIdx.x - run * (uint32_t)p.tiles) * rows;
+  *h0 = (int)run * kh;
+  *s = (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
+  return *s < nseqs;
+}
+
+// No-write kernel, one-token and packed routes: one CTA per (sequence, run
+// of kh heads of one group, row tile), placed by head_run_coords.  Sequences
+// longer than LMAX take the register form, head by head.
 template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, bool VARLEN>
 __global__ void __launch_bounds__(WARPS * 32, 5)
-    ssu_nowrite_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t seq0,
+    ssu_nowrite_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t nseqs,
                        int kh) {
   using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
   using L = typename Cfg::L;
@@ -514,9 +527,9 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
   __shared__ HeadSteps<8, LMAX> hsteps;
   __shared__ float G[LMAX][LMAX];
 
-  const int64_t s = seq0 + blockIdx.z;
-  const int h0 = (int)blockIdx.y * kh;
-  const int p0 = (int)blockIdx.x * ROWS;
+  int64_t s;
+  int h0, p0;
+  if (!head_run_coords(p, nseqs, kh, ROWS, &s, &h0, &p0)) return;
   int64_t r0, src;
   int len;
   bool read_ok;
@@ -732,17 +745,20 @@ struct StageView {
   const float (*gate)[ROWS];
 };
 
-// Calls that write state (packed chains, or one token): grid (row tiles, runs
-// of kh heads of one group, sequences).  The slot lookups, the chain's write
+// Calls that write state (packed chains, or one token): one CTA per
+// (sequence, run of kh heads of one group, row tile), placed by
+// head_run_coords.  The slot lookups, the chain's write
 // slots, B / C and the per-head dt' / dA table are formed once for the run;
 // each head's state tile lands in shared memory by cp.async, issued one head
 // ahead so it is in flight while the previous head computes; each head then
 // runs step_rows on the same staged values, with the same stores, as the bulk
 // kernels (so the same bits).  Chains longer than LMAX take the per-head block
 // (ssu_block_on), head by head.
+// 16-bit state: 64-row tiles hold 64 state values per thread, so three CTAs
+// per SM (up to 168 registers, no spills) rather than four.
 template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, bool VARLEN>
-__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
-    ssu_run_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t seq0,
+__global__ void __launch_bounds__(WARPS * 32, sizeof(ST) == 2 ? 3 : 16 / WARPS)
+    ssu_run_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t nseqs,
                    int kh) {
   using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
   using L = typename Cfg::L;
@@ -757,9 +773,9 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
   __shared__ HeadRows<ROWS, LMAX> hrows[2];
   __shared__ HeadSteps<8, LMAX> hsteps;
 
-  const int64_t s = seq0 + blockIdx.z;
-  const int h0 = (int)blockIdx.y * kh;
-  const int p0 = (int)blockIdx.x * ROWS;
+  int64_t s;
+  int h0, p0;
+  if (!head_run_coords(p, nseqs, kh, ROWS, &s, &h0, &p0)) return;
   int64_t r0, src;
   int len;
   bool read_ok;
@@ -793,14 +809,14 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     return;
   }
 
-  // the chain's write slots (the same for every head of the run)
-  int64_t dsts[LMAX];
-  bool dok[LMAX];
-#pragma unroll
-  for (int i = 0; i < LMAX; ++i) {
+  // the chain's write slots (the same for every head of the run), -1 where a
+  // step writes nothing; kept in shared memory, not in registers
+  __shared__ int64_t dsts[LMAX];
+  if (threadIdx.x < LMAX) {
+    const int i = threadIdx.x;
     int64_t v = -1;
-    dok[i] = i < len && read_ok && !p.disable && dst_of(i, &v) && slot_ok(v, p.pad, p.slots);
-    dsts[i] = v;
+    const bool ok = i < len && read_ok && !p.disable && dst_of(i, &v) && slot_ok(v, p.pad, p.slots);
+    dsts[i] = ok ? v : -1;
   }
 
   // 1. the first head's state tile by 16-byte async copies (each head's tile
@@ -875,8 +891,9 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     for (int tt = 0; tt < LMAX; ++tt) {
       if (tt >= len) break;
       step_rows<ST, IT, N, UNR>(hs, view, tt, q, jbase, p, h, p0, r0 + tt);
-      if (dok[tt]) {
-        ST* base = state + ((dsts[tt] * p.H + h) * block_elems);
+      const int64_t dst = dsts[tt];
+      if (dst >= 0) {
+        ST* base = state + ((dst * p.H + h) * block_elems);
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
           const int prow = p0 + (warp * UNR + u) * L::RPW + rr;

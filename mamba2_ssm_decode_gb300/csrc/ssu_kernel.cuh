@@ -227,28 +227,6 @@ __device__ __forceinline__ int bc_slot(int k) {
   return ((c * H4 + h) * L::LPR + q) * 4 + (k & 3);
 }
 
-// Load lane q's B and C values of step tt from the staged rows, as pairs
-// (pair e2 holds the lane's elements 2 e2 and 2 e2 + 1).
-template <class ST, int N, class StageT>
-__device__ __forceinline__ void lane_bc(const StageT& stg, int tt, int q, float2* bv, float2* cv) {
-  using L = RowLayout<ST, N>;
-  constexpr int H4 = L::VEC / 4;
-#pragma unroll
-  for (int c = 0; c < L::CPL; ++c) {
-#pragma unroll
-    for (int h = 0; h < H4; ++h) {
-      const int o = ((c * H4 + h) * L::LPR + q) * 4;
-      const float4 b4 = *reinterpret_cast<const float4*>(&stg.B[tt][o]);
-      const float4 c4 = *reinterpret_cast<const float4*>(&stg.C[tt][o]);
-      const int e2 = (c * L::VEC + 4 * h) / 2;
-      bv[e2] = make_float2(b4.x, b4.y);
-      bv[e2 + 1] = make_float2(b4.z, b4.w);
-      cv[e2] = make_float2(c4.x, c4.y);
-      cv[e2 + 1] = make_float2(c4.z, c4.w);
-    }
-  }
-}
-
 // Reduce-scatter of R per-row partial sums over the lanes of a row group:
 // at each offset (from LPR/2 down) a lane keeps half of its rows and sends
 // the other half to its partner, so after log2(R) exchanges every lane holds
@@ -284,32 +262,53 @@ struct RowScatter {
 // One step of the recurrence for this thread's UNR state rows (pairs in hs):
 //   h <- h dA + (dt' x) B;  y = sum_n h C + D x;  y *= silu(z)
 // with the row's B, C, dA, dt' x, D x, silu(z) read from the staged step tt.
-// Rows of the tile are jbase + u * RPW (u < UNR); y goes to out row r.
+// Rows of the tile are jbase + u * RPW (u < UNR); y goes to out row r.  The
+// lane's B and C are read one 16-byte chunk at a time (live registers for one
+// chunk, not the whole row); every row still sums its pairs in element order.
 template <class ST, class IT, int N, int UNR, class StageT>
 __device__ __forceinline__ void step_rows(float2 (&hs)[UNR][RowLayout<ST, N>::EPL / 2],
                                           const StageT& stg, int tt, int q, int jbase,
                                           const KParams& p, int h, int p0, int64_t r) {
   using L = RowLayout<ST, N>;
-  constexpr int E2 = L::EPL / 2;
-  float2 bv[E2], cv[E2];
-  lane_bc<ST, N>(stg, tt, q, bv, cv);
-  float acc[UNR];
+  constexpr int H4 = L::VEC / 4;
+  constexpr int C2 = L::VEC / 2;  // element pairs per chunk
+  float dA[UNR], dtx[UNR];
+  float2 a2[UNR];  // even and odd elements: two partial sums per row
 #pragma unroll
   for (int u = 0; u < UNR; ++u) {
     const int j = jbase + u * L::RPW;
-    const float dA = stg.dA[tt][j];
-    const float dtx = stg.dtx[tt][j];
-    const float2 dA2 = make_float2(dA, dA);
-    const float2 dtx2 = make_float2(dtx, dtx);
-    float2 a2 = make_float2(0.0f, 0.0f);  // even and odd elements: two partial sums
-#pragma unroll
-    for (int e2 = 0; e2 < E2; ++e2) {
-      const float2 hv = __ffma2_rn(hs[u][e2], dA2, __fmul2_rn(dtx2, bv[e2]));
-      hs[u][e2] = hv;
-      a2 = __ffma2_rn(hv, cv[e2], a2);
-    }
-    acc[u] = a2.x + a2.y;
+    dA[u] = stg.dA[tt][j];
+    dtx[u] = stg.dtx[tt][j];
+    a2[u] = make_float2(0.0f, 0.0f);
   }
+#pragma unroll
+  for (int c = 0; c < L::CPL; ++c) {
+    float2 bv[C2], cv[C2];
+#pragma unroll
+    for (int hh = 0; hh < H4; ++hh) {
+      const int o = ((c * H4 + hh) * L::LPR + q) * 4;
+      const float4 b4 = *reinterpret_cast<const float4*>(&stg.B[tt][o]);
+      const float4 c4 = *reinterpret_cast<const float4*>(&stg.C[tt][o]);
+      bv[2 * hh] = make_float2(b4.x, b4.y);
+      bv[2 * hh + 1] = make_float2(b4.z, b4.w);
+      cv[2 * hh] = make_float2(c4.x, c4.y);
+      cv[2 * hh + 1] = make_float2(c4.z, c4.w);
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const float2 dA2 = make_float2(dA[u], dA[u]);
+      const float2 dtx2 = make_float2(dtx[u], dtx[u]);
+#pragma unroll
+      for (int i = 0; i < C2; ++i) {
+        const float2 hv = __ffma2_rn(hs[u][c * C2 + i], dA2, __fmul2_rn(dtx2, bv[i]));
+        hs[u][c * C2 + i] = hv;
+        a2[u] = __ffma2_rn(hv, cv[i], a2[u]);
+      }
+    }
+  }
+  float acc[UNR];
+#pragma unroll
+  for (int u = 0; u < UNR; ++u) acc[u] = a2[u].x + a2[u].y;
   int base = 0, plain = 0;
   RowScatter<UNR, L::LPR / 2>::run(acc, q, base, plain);
   constexpr int LEFT = UNR > L::LPR ? UNR / L::LPR : 1;  // rows a lane still owns

@@ -175,48 +175,33 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
                   : launch_bulk<ST, IT, N, false>(p, o0, v0, nitems, stream);
   }
   if (nitems <= 0) return cudaSuccess;
-  // head-run kernels: grid (row tiles, runs of kh heads of one group,
-  // sequences); y / z extents are limited to 65535, so longer batches go in
-  // several launches of up to 65535 sequences
+  // head-run kernels: one launch whatever the batch; grid.x = runs of kh
+  // heads of one group x row tiles, sequences over grid.y x grid.z (each at
+  // most 65535, so z = ceil(nitems / 65535) and y = ceil(nitems / z) leave
+  // fewer than z idle CTAs)
   using NT = HeadRunTune<ST, N>;
   p.tiles = (p.P + NT::ROWS - 1) / NT::ROWS;
   set_divisors(p);
   const int kh = heads_per_cta(p.hr, nitems * p.H * (int64_t)p.tiles);
-  if (p.H / kh > 65535) return cudaErrorInvalidConfiguration;
+  const int64_t gx = (int64_t)(p.H / kh) * p.tiles;
+  const int64_t gz = (nitems + 65534) / 65535;
+  const int64_t gy = (nitems + gz - 1) / gz;
+  if (gx > 0x7fffffffLL || gz > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)gz);
   const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
   const VarlenArgs v0 = va ? *va : VarlenArgs{};
-  constexpr int64_t kZ = 65535;
-  if (p.disable) {
-    auto kern = varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
-                       : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
-    // several CTAs of up to 45 KB static shared memory per SM: ask for the
-    // largest shared-memory carveout
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    for (int64_t s0 = 0; s0 < nitems; s0 += kZ) {
-      const dim3 grid((unsigned)p.tiles, (unsigned)(p.H / kh),
-                      (unsigned)std::min(kZ, nitems - s0));
-      kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, s0, kh);
-      e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
-  }
-  auto kern = varlen ? ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
-                     : ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
-  // up to 45 KB of static shared memory per CTA: the largest carveout
+  auto kern = p.disable
+                  ? (varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
+                            : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>)
+                  : (varlen ? ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
+                            : ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>);
+  // several CTAs of up to 45 KB static shared memory per SM: ask for the
+  // largest shared-memory carveout
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  for (int64_t s0 = 0; s0 < nitems; s0 += kZ) {
-    const dim3 grid((unsigned)p.tiles, (unsigned)(p.H / kh),
-                    (unsigned)std::min(kZ, nitems - s0));
-    kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, s0, kh);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, nitems, kh);
+  return cudaGetLastError();
 }
 
 template <class ST, class IT>

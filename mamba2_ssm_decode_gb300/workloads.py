@@ -109,6 +109,14 @@ def _head_params(H, g, device):
     return A, D, dt_bias
 
 
+def _channel_params(H, P, g, device):
+    """A, D, dt_bias per (head, dim) channel [H, P], same distributions."""
+    A = -torch.exp(_uniform((H, P), 0.0, math.log(16.0), g, device))
+    D = _uniform((H, P), 0.0, 1.0, g, device)
+    dt_bias = _uniform((H, P), -4.0, -1.0, g, device)
+    return A, D, dt_bias
+
+
 def _distinct_slots(count, slots, g, device):
     if count > slots:
         raise ValueError(f"need {count} distinct slots from a pool of {slots}")
@@ -128,13 +136,14 @@ def _pad_some(table, npad, pad, g, device):
 def single_token_case(*, batch, heads, headdim, dstate, groups, slots, state_dtype,
                       io_dtype=torch.bfloat16, pad_frac=0.0, with_z=True, dt_per_dim=False,
                       index_dtype=torch.int32, identity_slots=False, disable_state_update=False,
-                      seed=0, device="cpu", name="single") -> SSUCase:
+                      per_channel=False, seed=0, device="cpu", name="single") -> SSUCase:
     g = _gen(seed, device)
     state = _normal((slots, heads, headdim, dstate), 0.1, state_dtype, g, device)
     x = _normal((batch, heads, headdim), 1.0, io_dtype, g, device)
     dt_shape = (batch, heads, headdim) if dt_per_dim else (batch, heads)
     dt = _normal(dt_shape, 1.0, torch.float32, g, device)
-    A, D, dt_bias = _head_params(heads, g, device)
+    A, D, dt_bias = (_channel_params(heads, headdim, g, device) if per_channel
+                     else _head_params(heads, g, device))
     B = _normal((batch, groups, dstate), 1.0, io_dtype, g, device)
     C = _normal((batch, groups, dstate), 1.0, io_dtype, g, device)
     z = _normal((batch, heads, headdim), 1.0, io_dtype, g, device) if with_z else None
@@ -248,6 +257,22 @@ def mtp_varlen(seed=0, device="cpu") -> SSUCase:
                        name="mtp-varlen-s128")
 
 
+def mamba2_2p7b_decode_perchannel(seed=0, device="cpu") -> SSUCase:
+    """The Mamba2-2.7B-shaped decode with A, D and dt_bias given per (head, dim)
+    channel ([80, 64] fp32; "mate.mamba" _per_head's channel-wise form)."""
+    return single_token_case(batch=256, heads=80, headdim=64, dstate=128, groups=1, slots=512,
+                             state_dtype=torch.float32, pad_frac=0.05, per_channel=True,
+                             seed=seed, device=device, name="mamba2-2.7b-decode-perchannel-b256")
+
+
+def mtp_varlen_dt_per_dim(seed=0, device="cpu") -> SSUCase:
+    """The packed varlen MTP workload with a full [rows, 80, 64] dt (one dt per
+    head and dim) instead of one per head."""
+    return varlen_case(nseqs=128, max_len=4, heads=80, headdim=64, dstate=128, groups=1,
+                       slots=1024, state_dtype=torch.float32, dt_per_dim=True, seed=seed,
+                       device=device, name="mtp-varlen-dtperdim-s128")
+
+
 def sweep_case(batch, state_dtype, mode, disable_state_update=False, seed=0,
                device="cpu") -> SSUCase:
     """Large-batch sweep point: 128 heads, headdim 64, dstate 128, 8 groups,
@@ -278,4 +303,80 @@ WORKLOADS = {
     "mamba2-2.7b-decode": mamba2_2p7b_decode,
     "hybrid-grouped-decode": hybrid_grouped_decode,
     "mtp-varlen": mtp_varlen,
+    "mamba2-2.7b-decode-perchannel": mamba2_2p7b_decode_perchannel,
+    "mtp-varlen-dtperdim": mtp_varlen_dt_per_dim,
 }
+
+
+# ---------------------------------------------------------------------------
+# selecting sequences of a case (no arithmetic: rows, slots and tables only)
+# ---------------------------------------------------------------------------
+
+def _slot_list(t):
+    return t.reshape(-1).tolist() if t is not None else []
+
+
+def sequence_rows(case, seqs):
+    """(packed rows, lengths) of the sequences `seqs` of a case."""
+    if case.kind == "single":
+        return list(seqs), [1] * len(seqs)
+    if case.cu_seqlens is not None:
+        cu = case.cu_seqlens.cpu().long().tolist()
+    else:
+        cu = [s * case.dense_steps for s in range(case.nseqs + 1)]
+    rows, lens = [], []
+    for s in seqs:
+        rows += list(range(cu[s], cu[s + 1]))
+        lens.append(cu[s + 1] - cu[s])
+    return rows, lens
+
+
+def subset_case(case, seqs):
+    """A compact CPU case of the sequences `seqs` of `case` (any device): their
+    rows, and their read / write slots copied into a small pool and renumbered.
+    Returns (case, rows, slot map old -> new).  Trackers are dropped."""
+    pad = case.pad_slot_id
+    slots_total = case.state.shape[0]
+    sbi = case.state_batch_indices.cpu() if case.state_batch_indices is not None else None
+    dsbi = (case.dst_state_batch_indices.cpu()
+            if case.dst_state_batch_indices is not None else None)
+    rows, lens = sequence_rows(case, seqs)
+    sel = torch.tensor(list(seqs), dtype=torch.long)
+    sub_sbi = sbi[sel] if sbi is not None else None
+    sub_dsbi = dsbi[sel] if dsbi is not None else None
+    if sbi is None:   # no read table: sequence s uses slot s
+        used_ids = list(seqs)
+    else:
+        used_ids = _slot_list(sub_sbi) + _slot_list(sub_dsbi)
+    used = sorted({v for v in used_ids if v != pad and 0 <= v < slots_total})
+    remap = {old: new for new, old in enumerate(used)}
+
+    def mapped(t):
+        if t is None:
+            return None
+        return t.clone().apply_(lambda v: remap.get(v, pad)).to(t.dtype)
+
+    dev = case.state.device
+    if used:
+        pool = case.state[torch.tensor(used, dtype=torch.long, device=dev)].cpu().contiguous()
+    else:   # a one-slot pool keeps the state tensor valid
+        pool = torch.zeros((1, *case.state.shape[1:]), dtype=case.state.dtype)
+    rws = torch.tensor(rows, dtype=torch.long, device=case.x.device)
+    pick = (lambda t: None if t is None else t[rws].cpu())
+    sub = dataclasses.replace(
+        case, state=pool, x=pick(case.x), dt=pick(case.dt), B=pick(case.B), C=pick(case.C),
+        z=pick(case.z), A=case.A.cpu(), D=None if case.D is None else case.D.cpu(),
+        dt_bias=None if case.dt_bias is None else case.dt_bias.cpu(),
+        state_batch_indices=mapped(sub_sbi) if sbi is not None else torch.tensor(
+            [remap.get(s, pad) for s in seqs], dtype=torch.int64),
+        dst_state_batch_indices=mapped(sub_dsbi), nseqs=len(seqs), ring_start=None,
+        prev_num_accepted=None, prev_query_len=None)
+    if case.kind == "varlen":
+        cu_new = [0]
+        for n in lens:
+            cu_new.append(cu_new[-1] + n)
+        sub.cu_seqlens = torch.tensor(cu_new, dtype=torch.int64)
+        sub.dense_steps = 1
+        sub.num_accepted_tokens = (None if case.num_accepted_tokens is None
+                                   else case.num_accepted_tokens.cpu()[sel])
+    return sub, rows, remap

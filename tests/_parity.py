@@ -13,8 +13,6 @@ Tolerances (the stated acceptance criteria, made concrete):
 """
 from __future__ import annotations
 
-import dataclasses
-
 import torch
 
 import mamba2_ssm_decode_gb300 as ssu
@@ -122,70 +120,46 @@ def parity(oracle, case_gpu, out_dtype=None, label="", algorithm="auto"):
     return {"y_err": ry, "state_err": rs, "slots_written": nchanged}
 
 
+def graph_kernel_nodes(fn):
+    """Kernel launches `fn` makes: capture it in a CUDA graph (nothing runs) and
+    count the graph's kernel nodes through the driver API."""
+    import ctypes
+    import pytest
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+    except TypeError:
+        pytest.skip("this torch cannot keep the captured graph")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()                      # set-up (attributes, lazy loading) outside the capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    cu = ctypes.CDLL("libcuda.so.1")
+    h = ctypes.c_void_p(g.raw_cuda_graph())
+    n = ctypes.c_size_t(0)
+    assert cu.cuGraphGetNodes(h, None, ctypes.byref(n)) == 0
+    nodes = (ctypes.c_void_p * max(1, n.value))()
+    assert cu.cuGraphGetNodes(h, nodes, ctypes.byref(n)) == 0
+    kernels = 0
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        assert cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0
+        kernels += t.value == 0   # CU_GRAPH_NODE_TYPE_KERNEL
+    del g
+    return kernels
+
+
 # ---------------------------------------------------------------------------
 # sampled parity for workloads too large to copy whole to the host
 # ---------------------------------------------------------------------------
 
-def _slot_list(t):
-    return t.reshape(-1).tolist() if t is not None else []
-
-
 def subset(case_gpu, seqs):
-    """A small CPU case holding only sequences `seqs` of a GPU case: their rows,
-    and their read / write slots remapped into a compact pool copied from the
-    GPU.  Returns (cpu_case, rows, slot_map old -> new)."""
-    pad = case_gpu.pad_slot_id
-    slots_total = case_gpu.state.shape[0]
-    sbi = case_gpu.state_batch_indices.cpu() if case_gpu.state_batch_indices is not None else None
-    dsbi = (case_gpu.dst_state_batch_indices.cpu()
-            if case_gpu.dst_state_batch_indices is not None else None)
-    if case_gpu.kind == "single":
-        rows = list(seqs)
-        lens = [1] * len(seqs)
-    else:
-        if case_gpu.cu_seqlens is not None:
-            cu = case_gpu.cu_seqlens.cpu().long().tolist()
-        else:
-            T = case_gpu.dense_steps
-            cu = [s * T for s in range(case_gpu.nseqs + 1)]
-        rows, lens = [], []
-        for s in seqs:
-            rows += list(range(cu[s], cu[s + 1]))
-            lens.append(cu[s + 1] - cu[s])
-    sel_s = torch.tensor(list(seqs), dtype=torch.long)
-    sub_sbi = sbi[sel_s] if sbi is not None else None
-    sub_dsbi = dsbi[sel_s] if dsbi is not None else None
-    used = sorted({v for v in _slot_list(sub_sbi) + _slot_list(sub_dsbi)
-                   if v != pad and 0 <= v < slots_total})
-    remap = {old: new for new, old in enumerate(used)}
-
-    def mapped(t):
-        if t is None:
-            return None
-        return t.clone().apply_(lambda v: remap.get(v, pad)).to(t.dtype)
-
-    pool = case_gpu.state[torch.tensor(used, dtype=torch.long, device=case_gpu.state.device)]
-    rws = torch.tensor(rows, dtype=torch.long, device=case_gpu.x.device)
-    pick = (lambda t: None if t is None else t[rws].cpu())
-    sub = dataclasses.replace(
-        case_gpu,
-        state=pool.cpu().contiguous(), x=pick(case_gpu.x), dt=pick(case_gpu.dt),
-        B=pick(case_gpu.B), C=pick(case_gpu.C), z=pick(case_gpu.z),
-        A=case_gpu.A.cpu(), D=None if case_gpu.D is None else case_gpu.D.cpu(),
-        dt_bias=None if case_gpu.dt_bias is None else case_gpu.dt_bias.cpu(),
-        state_batch_indices=mapped(sub_sbi), dst_state_batch_indices=mapped(sub_dsbi),
-        nseqs=len(seqs), ring_start=None, prev_num_accepted=None, prev_query_len=None)
-    if case_gpu.kind == "varlen":
-        cu_new = [0]
-        for L in lens:
-            cu_new.append(cu_new[-1] + L)
-        sub.cu_seqlens = torch.tensor(cu_new, dtype=torch.int64)
-        sub.dense_steps = 1
-        sub.num_accepted_tokens = (None if case_gpu.num_accepted_tokens is None
-                                   else case_gpu.num_accepted_tokens.cpu()[sel_s])
-    if not used:  # keep a one-slot pool so the oracle has a valid state tensor
-        sub.state = torch.zeros((1, *case_gpu.state.shape[1:]), dtype=case_gpu.state.dtype)
-    return sub, rows, remap
+    """A small CPU case holding only sequences `seqs` of a GPU case (their rows,
+    their slots copied into a compact pool); (cpu_case, rows, slot_map)."""
+    from mamba2_ssm_decode_gb300 import workloads as W
+    return W.subset_case(case_gpu, seqs)
 
 
 def sampled_parity(oracle, case_gpu, seqs, out_dtype=None, label="", algorithm="auto"):

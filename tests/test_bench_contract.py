@@ -70,5 +70,10 @@ def test_cuda_arm_line():
     assert d["gpu_launches"] == 20          # one SSU launch per timed step
     ck = d["clocks"]
     assert ck["sm_max_mhz"] > 0 and isinstance(ck["reasons"], list)
+    assert ck["samples_in_timed_region"] > 0     # the clock record covers the timed steps
+    assert d["device_error"] == 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
+    assert cb["single_core_value"] > 0
+    # the GPU step checked against the oracle on the sample, inside the tolerances
+    assert cb["parity"]["ok"] and cb["parity"]["sequences"] > 0

@@ -482,23 +482,36 @@ def test_workload_sweep_sampled(oracle_mod, b, sdt, mode, disable):
 
 
 # ---------------------------------------------------------------------------
-# more sequences than one launch of the head-run kernels holds
+# batches beyond the 65535 extent of one grid dimension
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("disable", [False, True])
-@pytest.mark.parametrize("kind", ["single", "varlen"])
-def test_more_sequences_than_one_launch(oracle_mod, kind, disable):
-    """The head-run kernels put sequences on the grid's z extent (at most 65535)
-    and split longer batches into several launches: every element on both sides
-    of the 65535-sequence boundary matches the oracle."""
+def _big_case(kind, disable, seed_offset=0):
     kw = dict(heads=1, headdim=16, dstate=16, groups=1, state_dtype=torch.float32,
               pad_frac=0.01, disable_state_update=disable, device=DEV)
     if kind == "single":
-        case = W.single_token_case(batch=70001, slots=70010, seed=71, **kw)
-    else:
-        case = W.varlen_case(nseqs=66000, max_len=2, slots=132010, same_tables=True, seed=72,
-                             **kw)
-    r = P.parity(oracle_mod, case, label=f"{kind} disable={disable} beyond one launch",
+        return W.single_token_case(batch=70001, slots=70010, seed=71 + seed_offset, **kw)
+    return W.varlen_case(nseqs=66000, max_len=2, slots=132010, same_tables=True,
+                         seed=72 + seed_offset, **kw)
+
+
+@pytest.mark.parametrize("disable", [False, True])
+@pytest.mark.parametrize("kind", ["single", "varlen"])
+def test_more_sequences_than_one_grid_dimension(oracle_mod, kind, disable):
+    """The head-run kernels spread sequences over two grid dimensions: every
+    element on both sides of the 65535-sequence boundary matches the oracle."""
+    case = _big_case(kind, disable)
+    r = P.parity(oracle_mod, case, label=f"{kind} disable={disable} beyond 65535 sequences",
                  algorithm="direct")
     if not disable:
         assert r["slots_written"] > 65535
+
+
+@pytest.mark.parametrize("algo", ["auto", "direct", "bulk"])
+@pytest.mark.parametrize("disable", [False, True])
+@pytest.mark.parametrize("kind", ["single", "varlen"])
+def test_every_call_is_one_launch(kind, disable, algo):
+    """Each SSU call issues exactly one kernel launch, whatever the batch: the
+    call captured in a CUDA graph holds one kernel node (70001 one-token
+    sequences, 66000 packed sequences)."""
+    case = _big_case(kind, disable, seed_offset=100)
+    assert P.graph_kernel_nodes(lambda: P.run_gpu(case, algorithm=algo)) == 1
