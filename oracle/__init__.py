@@ -28,7 +28,7 @@ _lock = threading.Lock()
 _lib = None
 
 # dtype codes of the C interface (ssu_oracle.c's own enum)
-_DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+_DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.float64: 3}
 
 _p = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -75,6 +75,17 @@ def _load():
             lib.oracle_ring_commit.restype = _int
             lib.oracle_ring_commit.argtypes = (
                 [_p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _i32, _i32, _i64])
+            lib.oracle_replay_update.restype = _int
+            lib.oracle_replay_update.argtypes = (
+                [_p, _int, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
+                 _p, _p, _int, _p, _p, _p, _p, _p, _p,
+                 _p, _p, _i64,
+                 _p, _p, _p, _i64,
+                 _p, _p, _i64, _i32, _int, _int, _int, _p])
+            lib.oracle_replay_state.restype = _int
+            lib.oracle_replay_state.argtypes = (
+                [_p, _int, _i64, _i64, _i64, _i64, _i64, _int, _p, _p, _int, _int,
+                 _i64, _p, _p, _p, _i64, _p, _p, _i64, _p])
             lib.oracle_encode.restype = None
             lib.oracle_encode.argtypes = [_p, _i64, _int, _p]
             lib.oracle_decode.restype = None
@@ -265,6 +276,85 @@ def ring_commit(ring_start, prev_num_accepted, prev_query_len, state_batch_indic
         nseqs, int(logical_window), int(ring_buffer_len), int(pad_slot_id))
     if rc != 0:
         raise ValueError(f"oracle_ring_commit rejected its arguments (code {rc})")
+
+
+def _replay_caches(x_cache, B_cache, dt_cache, ring_start, prev_num_accepted, io):
+    for name, t in (("x_cache", x_cache), ("B_cache", B_cache)):
+        assert t.device.type == "cpu" and t.is_contiguous() and t.dim() == 4, name
+        assert _DT[t.dtype] == io, f"{name} must have the x dtype"
+    assert dt_cache.device.type == "cpu" and dt_cache.is_contiguous()
+    assert dt_cache.dtype == torch.float32 and dt_cache.dim() == 3
+    for t in (ring_start, prev_num_accepted):
+        assert t.device.type == "cpu" and t.dtype == torch.int32 and t.is_contiguous()
+    return x_cache.shape[2], min(ring_start.numel(), prev_num_accepted.numel())
+
+
+def replay_update(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, ring_start,
+                  prev_num_accepted, logical_window, D=None, z=None, dt_bias=None,
+                  dt_softplus=False, cu_seqlens=None, state_batch_indices=None, pad_slot_id=-1,
+                  update_trackers=True, nseqs=None):
+    """ReplaySSM checkpointing update on CPU tensors (ssu_oracle.c,
+    oracle_replay_update: the readings are stated there).
+
+    state [slots, H, P, N] (checkpoints; fp32/bf16/fp16, or fp64 for pins), the
+    caches x_cache [slots, H, R, P], B_cache [slots, G, R, N] (x dtype) and
+    dt_cache [slots, H, R] fp32, the int32 trackers ring_start and
+    prev_num_accepted: all updated IN PLACE.  x, z [rows, H, P]; dt [rows, H];
+    B, C [rows, G, N]; cu_seqlens [S + 1] or None (one row per sequence);
+    state_batch_indices [S] (slot per sequence) or None (slot s).  Returns y
+    float64 [rows, H, P]."""
+    lib = _load()
+    assert state.device.type == "cpu" and state.is_contiguous()
+    slots, H, P, N = state.shape
+    rows = x.shape[0]
+    G = B.shape[1]
+    io = _check_io(x, z, B, C)
+    R, num_states = _replay_caches(x_cache, B_cache, dt_cache, ring_start, prev_num_accepted,
+                                   io)
+    x, z, B, C = _cpu(x), _cpu(z), _cpu(B), _cpu(C)
+    dt = _cpu(dt, torch.float32)
+    if dt.dim() == 3:
+        assert dt.shape[2] == 1, "ReplaySSM caches one dt per head"
+        dt = dt[:, :, 0].contiguous()
+    A, D, dt_bias, per_dim = _params(A, D, dt_bias, H, P)
+    cu = _cpu(cu_seqlens, torch.int64)
+    if nseqs is None:
+        nseqs = cu.numel() - 1 if cu is not None else rows
+    sbi = _cpu(state_batch_indices, torch.int64)
+    if sbi is not None:
+        sbi = sbi.reshape(sbi.shape[0], -1)[:, 0].contiguous()   # column 0 of a 2-D table
+    y = torch.full((rows, H, P), float("nan"), dtype=torch.float64)
+    rc = lib.oracle_replay_update(
+        _ptr(state), _DT[state.dtype], slots, H, P, N, G, nseqs, rows,
+        _ptr(x), _ptr(z), io, _ptr(dt), _ptr(A), _ptr(D), _ptr(dt_bias), _ptr(B), _ptr(C),
+        _ptr(cu), _ptr(sbi), int(pad_slot_id),
+        _ptr(x_cache), _ptr(B_cache), _ptr(dt_cache), R,
+        _ptr(ring_start), _ptr(prev_num_accepted), num_states, int(logical_window),
+        int(bool(update_trackers)), int(bool(dt_softplus)), per_dim, _ptr(y))
+    if rc != 0:
+        raise ValueError(f"oracle_replay_update rejected its arguments (code {rc})")
+    return y
+
+
+def replay_state(state, slot, A, x_cache, B_cache, dt_cache, ring_start, prev_num_accepted,
+                 dt_bias=None, dt_softplus=False):
+    """The logical state of one slot (checkpoint advanced through its cached
+    tokens) as float64 [H, P, N]; nothing is written."""
+    lib = _load()
+    slots, H, P, N = state.shape
+    G = B_cache.shape[1]
+    io = _DT[x_cache.dtype]
+    R, num_states = _replay_caches(x_cache, B_cache, dt_cache, ring_start, prev_num_accepted,
+                                   io)
+    A, _, dt_bias, per_dim = _params(A, None, dt_bias, H, P)
+    out = torch.empty((H, P, N), dtype=torch.float64)
+    rc = lib.oracle_replay_state(
+        _ptr(state), _DT[state.dtype], slots, H, P, N, G, io, _ptr(A), _ptr(dt_bias),
+        int(bool(dt_softplus)), per_dim, int(slot), _ptr(x_cache), _ptr(B_cache), _ptr(dt_cache),
+        R, _ptr(ring_start), _ptr(prev_num_accepted), num_states, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_replay_state: slot {slot} has out-of-range trackers")
+    return out
 
 
 def round_to(values: torch.Tensor, dtype: torch.dtype) -> torch.Tensor:

@@ -37,15 +37,20 @@
  * round-to-nearest-even, from the double value to the state dtype.  A chained
  * multi-token run keeps the unrounded double state between its steps.
  *
- * Readings where the pages are silent are listed at each function.
+ * Readings where the pages are silent are listed at each function.  The
+ * ReplaySSM checkpointing update (oracle_replay_update, at the end) reuses
+ * ssu_step for every replayed and every new token.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
-/* dtype codes used by this file's interface (its own; not shared) */
-enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2 };
+/* dtype codes used by this file's interface (its own; not shared).  OR_F64 is
+ * accepted for the state only: an fp64 pool (rounding is then the identity)
+ * lets the pins compare chains that store state with chains that do not, bit
+ * for bit. */
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2, OR_F64 = 3 };
 
 /* ------------------------------------------------------------------------ */
 /* exact widening of stored values                                          */
@@ -79,6 +84,7 @@ static double load_value(const void* base, int64_t i, int dtype) {
     case OR_F32: return (double)((const float*)base)[i];
     case OR_BF16: return bf16_bits_to_double(((const uint16_t*)base)[i]);
     case OR_F16: return f16_bits_to_double(((const uint16_t*)base)[i]);
+    case OR_F64: return ((const double*)base)[i];
   }
   return NAN;
 }
@@ -148,6 +154,7 @@ static void store_rounded(void* base, int64_t i, int dtype, double v) {
     case OR_F32: ((float*)base)[i] = (float)v; break;
     case OR_BF16: ((uint16_t*)base)[i] = exact_double_to_bf16_bits(oracle_round_bf16(v)); break;
     case OR_F16: ((uint16_t*)base)[i] = exact_double_to_f16_bits(oracle_round_f16(v)); break;
+    case OR_F64: ((double*)base)[i] = v; break;
   }
 }
 
@@ -432,5 +439,193 @@ int oracle_ring_commit(int32_t* ring_start, int64_t n_ring_start,
     prev_num_accepted[slot] = next_prev;
     prev_query_len[slot] = qlen;
   }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* ReplaySSM checkpointing update                                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * ReplaySSM ("ssu_dispatch": selective_state_update_replayssm_flashinfer, the
+ * FlashInfer checkpointing_ssu call it wraps, and the ring semantics of the
+ * tracker kernels above).  The pages fix the interface -- a checkpoint
+ * `state`, per-slot rings x_cache / B_cache / dt_cache of ring_len positions,
+ * ring_start and prev_num_accepted per slot, a logical window -- and where the
+ * trackers move the ring, not the arithmetic.  Readings:
+ *
+ *  - the logical state of a slot is its checkpoint state[slot] advanced, in
+ *    order, through the k = prev_num_accepted[slot] cached tokens at ring
+ *    positions (ring_start[slot] + j) mod ring_len, j < k; a cached token is
+ *    x [H, P], B [G, N] and dt [H] as the caller gave them (dt before dt_bias
+ *    and softplus), and its step is the plain step of ssu_step with the call's
+ *    A, dt_bias and dt_softplus;
+ *  - the call's L rows of the sequence continue the chain from the logical
+ *    state (y from the unrounded state, as in the plain calls); row t is cached
+ *    at position (ring_start + k + t) mod ring_len;
+ *  - when k + L exceeds the logical window, the state after the k replayed
+ *    tokens -- the state the trackers' new ring start (ring_start + k) names --
+ *    is rounded to the state dtype and written to state[slot];
+ *  - a sequence is processed when its slot is neither the pad id nor outside
+ *    [0, min(slots, num_states)), it has at least one row, and its trackers are
+ *    in range (0 <= k, k + L <= ring_len, 0 <= ring_start < ring_len); any
+ *    other sequence runs its rows from a zero state and writes nothing;
+ *  - update_trackers applies the one-token tracker rule of
+ *    oracle_ring_update (what the wrapper runs after the kernel) to the slot of
+ *    every processed sequence, after the call.
+ *
+ * Layouts (contiguous): x_cache, B_cache in the io dtype, [slots, H, R, P] and
+ * [slots, G, R, N]; dt_cache fp32 [slots, H, R]; R = ring_len.  dt is per head
+ * [rows, H].  Rows of sequence s: [cu[s], cu[s+1]), or the single row s when
+ * cu_seqlens is NULL.  Read/write slot of sequence s: sbi[s] (s when NULL).
+ */
+static void copy_io(void* dst, int64_t di, const void* src, int64_t si, int io_dtype) {
+  (void)io_dtype; /* bf16 and fp16 both move as 16-bit patterns */
+  ((uint16_t*)dst)[di] = ((const uint16_t*)src)[si];
+}
+
+static int replay_ok(int64_t slot, int64_t pad, int64_t limit, int32_t k, int32_t start,
+                     int64_t L, int64_t R) {
+  return slot != pad && slot >= 0 && slot < limit && L > 0 && k >= 0 && start >= 0 &&
+         start < R && (int64_t)k + L <= R;
+}
+
+/* Advance hb (head h of `slot`) through the cached token at ring position pos:
+ * the token's x, B, dt become a one-row operand set and take one plain step. */
+static void replay_token(const operands* o, int64_t h, const void* x_cache, const void* B_cache,
+                         const float* dt_cache, int64_t slot, int64_t pos, int64_t R,
+                         void* xrow, void* Brow, float* dtrow, double* ydump, double* hb) {
+  const int64_t H = o->H, P = o->P, N = o->N, G = o->G;
+  const int64_t g = h / (H / G);
+  for (int64_t p = 0; p < P; ++p) copy_io(xrow, h * P + p, x_cache, ((slot * H + h) * R + pos) * P + p, o->io_dtype);
+  for (int64_t n = 0; n < N; ++n) copy_io(Brow, g * N + n, B_cache, ((slot * G + g) * R + pos) * N + n, o->io_dtype);
+  dtrow[h] = dt_cache[(slot * H + h) * R + pos];
+  operands t = *o;
+  t.x = xrow;
+  t.B = Brow;
+  t.C = Brow; /* y of a replayed token is not kept */
+  t.z = NULL;
+  t.dt = dtrow;
+  t.dt_per_dim = 0;
+  ssu_step(&t, 0, h, hb, ydump);
+}
+
+int oracle_replay_update(void* state, int state_dtype, int64_t slots,
+                         int64_t H, int64_t P, int64_t N, int64_t G, int64_t nseqs, int64_t rows,
+                         const void* x, const void* z, int io_dtype, const float* dt,
+                         const float* A, const float* D, const float* dt_bias,
+                         const void* B, const void* C,
+                         const int64_t* cu_seqlens, const int64_t* sbi, int64_t pad_slot_id,
+                         void* x_cache, void* B_cache, float* dt_cache, int64_t ring_len,
+                         int32_t* ring_start, int32_t* prev_num_accepted, int64_t num_states,
+                         int32_t logical_window, int update_trackers, int dt_softplus,
+                         int param_per_dim, double* y) {
+  if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0 || ring_len < 1) return 1;
+  operands o = {H, P, N, G, x, z, io_dtype, dt, 0, A, D, dt_bias, B, C, dt_softplus,
+                param_per_dim};
+  const int64_t block = P * N;
+  const int64_t limit = slots < num_states ? slots : num_states;
+  double* hb = (double*)malloc(sizeof(double) * (size_t)block);
+  void* xrow = calloc((size_t)(H * P), 2);
+  void* Brow = calloc((size_t)(G * N), 2);
+  float* dtrow = (float*)calloc((size_t)H, sizeof(float));
+  double* ydump = (double*)malloc(sizeof(double) * (size_t)(H * P));
+  int32_t* processed = (int32_t*)calloc((size_t)(nseqs > 0 ? nseqs : 1), sizeof(int32_t));
+  if (!hb || !xrow || !Brow || !dtrow || !ydump || !processed) return 2;
+  for (int64_t s = 0; s < nseqs; ++s) {
+    int64_t begin = cu_seqlens ? cu_seqlens[s] : s;
+    int64_t end = cu_seqlens ? cu_seqlens[s + 1] : s + 1;
+    if (begin < 0) begin = 0;
+    if (end > rows) end = rows;
+    const int64_t L = end - begin;
+    if (L <= 0) continue;
+    const int64_t slot = sbi ? sbi[s] : s;
+    const int slot_valid = slot != pad_slot_id && slot >= 0 && slot < limit;
+    const int32_t k = slot_valid ? prev_num_accepted[slot] : 0;
+    const int32_t start = slot_valid ? ring_start[slot] : 0;
+    const int ok = replay_ok(slot, pad_slot_id, limit, k, start, L, ring_len);
+    const int checkpoint = ok && (int64_t)k + L > logical_window;
+    processed[s] = ok;
+    for (int64_t h = 0; h < H; ++h) {
+      const int64_t off = (slot * H + h) * block;
+      for (int64_t i = 0; i < block; ++i) hb[i] = ok ? load_value(state, off + i, state_dtype) : 0.0;
+      if (ok) {
+        for (int32_t j = 0; j < k; ++j)
+          replay_token(&o, h, x_cache, B_cache, dt_cache, slot, ((int64_t)start + j) % ring_len,
+                       ring_len, xrow, Brow, dtrow, ydump, hb);
+        if (checkpoint)
+          for (int64_t i = 0; i < block; ++i) store_rounded(state, off + i, state_dtype, hb[i]);
+      }
+      for (int64_t t = 0; t < L; ++t) {
+        const int64_t r = begin + t;
+        ssu_step(&o, r, h, hb, y);
+        if (!ok) continue;
+        const int64_t pos = ((int64_t)start + k + t) % ring_len;
+        for (int64_t p = 0; p < P; ++p)
+          copy_io(x_cache, ((slot * H + h) * ring_len + pos) * P + p, x, (r * H + h) * P + p,
+                  io_dtype);
+        dt_cache[(slot * H + h) * ring_len + pos] = dt[r * H + h];
+        if (h % (H / G) == 0) { /* B of the group, once per group */
+          const int64_t g = h / (H / G);
+          for (int64_t n = 0; n < N; ++n)
+            copy_io(B_cache, ((slot * G + g) * ring_len + pos) * N + n, B, (r * G + g) * N + n,
+                    io_dtype);
+        }
+      }
+    }
+  }
+  int rc = 0;
+  if (update_trackers) {
+    for (int64_t s = 0; s < nseqs && rc == 0; ++s) {
+      if (!processed[s]) continue;
+      const int64_t slot = sbi ? sbi[s] : s;
+      rc = oracle_ring_update(ring_start, num_states, prev_num_accepted, num_states,
+                              prev_num_accepted /* prev_query_len: untouched by the rule */,
+                              num_states, &slot, 1, 1, 0, logical_window, (int32_t)ring_len,
+                              pad_slot_id);
+    }
+  }
+  free(hb);
+  free(xrow);
+  free(Brow);
+  free(dtrow);
+  free(ydump);
+  free(processed);
+  return rc;
+}
+
+/* The logical state of `slot` (its checkpoint advanced through its k ring
+ * entries, the first part of oracle_replay_update) as double [H, P, N]; the
+ * trackers are read, nothing is written.  Returns nonzero for a slot whose
+ * trackers are out of range (then out is left alone). */
+int oracle_replay_state(const void* state, int state_dtype, int64_t slots,
+                        int64_t H, int64_t P, int64_t N, int64_t G, int io_dtype,
+                        const float* A, const float* dt_bias, int dt_softplus, int param_per_dim,
+                        int64_t slot, const void* x_cache, const void* B_cache,
+                        const float* dt_cache, int64_t ring_len, const int32_t* ring_start,
+                        const int32_t* prev_num_accepted, int64_t num_states, double* out) {
+  const int64_t limit = slots < num_states ? slots : num_states;
+  if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0 || ring_len < 1) return 1;
+  if (slot < 0 || slot >= limit) return 1;
+  const int32_t k = prev_num_accepted[slot], start = ring_start[slot];
+  if (k < 0 || k > ring_len || start < 0 || start >= ring_len) return 1;
+  operands o = {H, P, N, G, NULL, NULL, io_dtype, NULL, 0, A, NULL, dt_bias, NULL, NULL,
+                dt_softplus, param_per_dim};
+  void* xrow = calloc((size_t)(H * P), 2);
+  void* Brow = calloc((size_t)(G * N), 2);
+  float* dtrow = (float*)calloc((size_t)H, sizeof(float));
+  double* ydump = (double*)malloc(sizeof(double) * (size_t)(H * P));
+  if (!xrow || !Brow || !dtrow || !ydump) return 2;
+  for (int64_t h = 0; h < H; ++h) {
+    double* hb = out + h * P * N;
+    for (int64_t i = 0; i < P * N; ++i) hb[i] = load_value(state, (slot * H + h) * P * N + i, state_dtype);
+    for (int32_t j = 0; j < k; ++j)
+      replay_token(&o, h, x_cache, B_cache, dt_cache, slot, ((int64_t)start + j) % ring_len,
+                   ring_len, xrow, Brow, dtrow, ydump, hb);
+  }
+  free(xrow);
+  free(Brow);
+  free(dtrow);
+  free(ydump);
   return 0;
 }

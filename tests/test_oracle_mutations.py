@@ -37,6 +37,23 @@ MUTANTS = {
                                  "(o->param_per_dim & 1) ? o->A[p * H + h]"),
     "bf16_truncates": ("double r = nearbyint(fabs(v) / quantum) * quantum;",
                        "double r = floor(fabs(v) / quantum) * quantum;"),
+    # ReplaySSM
+    "replay_checkpoint_at_window": ("const int checkpoint = ok && (int64_t)k + L > logical_window;",
+                                    "const int checkpoint = ok && (int64_t)k + L >= logical_window;"),
+    "replay_checkpoint_skipped": ("        if (checkpoint)\n", "        if (0 && checkpoint)\n"),
+    "replay_new_position_without_k": ("const int64_t pos = ((int64_t)start + k + t) % ring_len;",
+                                      "const int64_t pos = ((int64_t)start + t) % ring_len;"),
+    "replay_one_token_short": ("        for (int32_t j = 0; j < k; ++j)\n          replay_token(",
+                               "        for (int32_t j = 0; j + 1 < k; ++j)\n          replay_token("),
+    "replay_ring_start_ignored": (
+        "          replay_token(&o, h, x_cache, B_cache, dt_cache, slot, ((int64_t)start + j) % ring_len,",
+        "          replay_token(&o, h, x_cache, B_cache, dt_cache, slot, ((int64_t)j) % ring_len,"),
+    "replay_caches_biased_dt": ("dt_cache[(slot * H + h) * ring_len + pos] = dt[r * H + h];",
+                                "dt_cache[(slot * H + h) * ring_len + pos] = dt[r * H + h] + "
+                                "(dt_bias ? dt_bias[h] : 0.0f);"),
+    "replay_B_of_first_group": ("B, (r * G + g) * N + n,", "B, (r * G + 0) * N + n,"),
+    "replay_trackers_for_unprocessed": ("      if (!processed[s]) continue;\n",
+                                        "      (void)processed;\n"),
 }
 
 
@@ -53,6 +70,7 @@ def test_pins_catch_mutant(name, tmp_path):
     env = dict(os.environ, ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_trackers.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_trackers.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_replay.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
