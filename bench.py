@@ -59,6 +59,55 @@ def _esize(t):
     return 0 if t is None else t.element_size()
 
 
+def replay_accounting(case):
+    """(tokens, algorithmic bytes, 0) of a ReplaySSM checkpointing call.
+
+    Per processed sequence (valid slot, trackers in range) and head: the
+    checkpoint read, a checkpoint write when k + L > W, the k cached tokens' x
+    and dt read from the ring and the L new ones written to it; per group the
+    cached / new B; per row x, z, dt, B, C read and y written; the trackers (8
+    bytes read, 8 more written with the update) and the slot vector.  With the
+    tracker update in the call, k cycles through 1..W from call to call, so the
+    count is the mean over one cycle of W calls (exact for a multiple of W
+    timed calls)."""
+    slots, H, P, N, G = case.dims
+    sb = case.state.element_size()
+    io = case.x.element_size()
+    R, W = case.ring_buffer_len, case.logical_window
+    sbi = case.state_batch_indices.cpu().long() if case.state_batch_indices is not None else None
+    if case.cu_seqlens is not None:
+        cu = case.cu_seqlens.cpu().long().tolist()
+    else:
+        cu = list(range(case.nseqs + 1))
+    pna = case.prev_num_accepted.cpu().long().tolist()
+    rs = case.ring_start.cpu().long().tolist()
+    limit = min(slots, len(pna), len(rs))
+    seqs = []
+    for s in range(case.nseqs):
+        L = cu[s + 1] - cu[s]
+        slot = int(sbi[s]) if sbi is not None else s
+        if L <= 0 or slot == case.pad_slot_id or not 0 <= slot < limit:
+            continue
+        k, st = pna[slot], rs[slot]
+        if k < 0 or k + L > R or not 0 <= st < R:
+            continue
+        seqs.append((L, k))
+    phases = W if case.update_trackers and W >= 1 else 1
+    total = 0
+    for _ in range(phases):
+        for L, k in seqs:
+            total += H * P * N * sb * (1 + (k + L > W))
+            total += (k + L) * (H * P * io + H * 4 + G * N * io)
+            total += 8 + (8 if case.update_trackers else 0)
+        if phases > 1:
+            seqs = [(L, 1 if k + 1 > W else k + 1) for L, k in seqs]
+    per_row = H * P * io * (3 if case.z is not None else 2) + H * 4 + 2 * G * N * io
+    meta = sum(t.numel() * t.element_size() for t in (case.state_batch_indices, case.cu_seqlens)
+               if t is not None)
+    tokens = sum(L for L, _ in seqs)
+    return tokens, total // phases + case.rows * per_row + meta, 0
+
+
 def accounting(case):
     """(non-pad tokens, algorithmic bytes of the SSU launch, tracker bytes).
 
@@ -66,6 +115,8 @@ def accounting(case):
     its H x P x N state block once and writes it once per valid destination
     write; every packed row reads x, z, dt, B, C and writes y; plus the index
     tables and metadata (read once).  Pad sequences move no state."""
+    if case.kind == "replay":
+        return replay_accounting(case)
     slots, H, P, N, G = case.dims
     sb = case.state.element_size()
     block = H * P * N * sb
@@ -148,7 +199,11 @@ class Step:
         self.case = case
         self.algorithm = algorithm
         self.out = torch.empty_like(case.x)
-        self.launches = 1 + (2 if case.ring_start is not None else 0)
+        self.replay = case.kind == "replay"
+        # the replay call runs its tracker update itself (counters in scratch)
+        self.launches = 1 + (2 if case.ring_start is not None and not self.replay else 0)
+        self.scratch = (torch.zeros(max(1, case.nseqs), dtype=torch.int32, device=case.x.device)
+                        if self.replay else None)
         if case.kind == "varlen" and case.cu_seqlens is None:
             S, T = case.nseqs, case.dense_steps
 
@@ -172,6 +227,14 @@ class Step:
         c = self.case
         t = {n: over[n] if over.get(n) is not None else getattr(c, n) for n in self.STEP_INPUTS}
         out = self.out if out is None else out
+        if self.replay:
+            self.ssu.ssu_replay_update(
+                c.state, t["x"], t["dt"], c.A, t["B"], t["C"], c.x_cache, c.B_cache, c.dt_cache,
+                c.ring_start, c.prev_num_accepted, c.logical_window, D=c.D, z=t["z"],
+                dt_bias=c.dt_bias, dt_softplus=c.dt_softplus, cu_seqlens=t["cu_seqlens"],
+                state_batch_indices=t["state_batch_indices"], pad_slot_id=c.pad_slot_id, out=out,
+                update_trackers=c.update_trackers, scratch=self.scratch)
+            return
         kw = dict(D=c.D, z=t["z"], dt_bias=c.dt_bias, dt_softplus=c.dt_softplus,
                   pad_slot_id=c.pad_slot_id, disable_state_update=c.disable_state_update,
                   out=out, algorithm=self.algorithm)
@@ -197,7 +260,7 @@ class Step:
 
     def trackers(self, **over):
         c = self.case
-        if c.ring_start is None:
+        if c.ring_start is None or self.replay:
             return
         t = {n: over[n] if over.get(n) is not None else getattr(c, n) for n in self.STEP_INPUTS}
         sbi = t["state_batch_indices"]
@@ -569,7 +632,7 @@ def measure(name, device, seed, steps, warmup, stream, algorithm="auto"):
 # ---------------------------------------------------------------------------
 
 DEFAULT_WORKLOAD = "mamba2-2.7b-decode"
-EXTRAS = ["hybrid-grouped-decode", "mtp-varlen",
+EXTRAS = ["hybrid-grouped-decode", "mtp-varlen", "replay-decode", "replay-mtp",
           "mamba2-2.7b-decode-perchannel", "mtp-varlen-dtperdim",
           "sweep-single-float32-b1024", "sweep-single-bfloat16-b1024",
           "sweep-mtp-float32-b1024", "sweep-mtp-bfloat16-b1024",

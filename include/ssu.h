@@ -29,7 +29,8 @@
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
  *     allocates nothing and never copies device data to the host.  Each
  *     compute or tracker call (ssu_update, ssu_update_varlen,
- *     ssu_ring_update, ssu_ring_commit) issues exactly one kernel launch on
+ *     ssu_replay_update, ssu_ring_update, ssu_ring_commit) issues exactly
+ *     one kernel launch on
  *     `stream` (a cudaStream_t; NULL is the legacy default stream), whatever
  *     the batch, and never synchronises, so it can be captured in a CUDA
  *     graph.  The two diagnostic calls (ssu_device_error,
@@ -277,6 +278,75 @@ ssu_status ssu_ring_commit(int32_t* ring_start, int64_t ring_start_len,
                            int64_t pad_slot_id, struct CUstream_st* stream);
 
 /*
+ * ReplaySSM ring caches and trackers of a checkpointing update
+ * ("ssu_dispatch": selective_state_update_replayssm_flashinfer, the FlashInfer
+ * checkpointing_ssu call it wraps; ring semantics of
+ * _update_/_commit_replayssm_ring_trackers_kernel).  All device memory owned
+ * by the caller, contiguous; R = ring_len positions per slot.
+ *   x_cache            [slots, nheads, R, headdim], io_dtype
+ *   B_cache            [slots, ngroups, R, dstate], io_dtype
+ *   dt_cache           [slots, nheads, R], fp32 (dt as given: before dt_bias
+ *                      and softplus)
+ *   ring_start, prev_num_accepted   int32 trackers indexed by slot, at least
+ *                      num_states entries each (prev_query_len is not used:
+ *                      the one-token tracker rule leaves it unchanged)
+ *   logical_window     W: a checkpoint is written when k + L > W
+ */
+typedef struct ssu_replay_cache {
+  void* x_cache;
+  void* B_cache;
+  float* dt_cache;
+  int64_t ring_len;
+  int32_t* ring_start;
+  int32_t* prev_num_accepted;
+  int64_t num_states;
+  int32_t logical_window;
+} ssu_replay_cache;
+
+/*
+ * ReplaySSM checkpointing update (one launch).  state[slot] holds a
+ * checkpoint; the slot's state is the checkpoint advanced through the
+ * k = prev_num_accepted[slot] tokens cached at ring positions
+ * (ring_start[slot] + j) mod R, j < k.  For every sequence s (slot
+ * state_batch_indices[s], or s when NULL; rows [cu[s], cu[s+1]), or row s
+ * when cu_seqlens is NULL -- then rows == nseqs):
+ *   1. replay the k cached tokens (the plain recurrence with this call's A,
+ *      dt_bias, dt_softplus) from the checkpoint;
+ *   2. if k + L > logical_window, round that state to the state dtype and
+ *      write it to state[slot] (the new checkpoint);
+ *   3. run the L rows as the plain update does (y into out; z gate; D), and
+ *      cache row t's x, B and dt at ring position (ring_start + k + t) mod R;
+ *   4. with update_trackers, apply ssu_ring_update's one-token rule to the
+ *      slot (what the pages' wrapper runs after the kernel), in this launch.
+ *      MTP callers pass 0 and call ssu_ring_commit on their next pass.
+ * A sequence is skipped (rows from a zero state, nothing written: no
+ * checkpoint, ring entry or tracker) when its slot is pad_slot_id or outside
+ * [0, min(slots, num_states)), when it has no rows, or when its trackers are
+ * out of range (k < 0, k + L > R, ring_start outside [0, R)).  A ring of
+ * max(W, longest pass) + longest pass positions holds every pass after a
+ * commit.
+ *   p                 operands as for ssu_update_varlen; dt must be per head
+ *                     (dt_dim_stride 0: the ring caches one dt per head),
+ *                     disable_state_update must be 0; p->algorithm is ignored.
+ *   meta_dtype        I32 / I64 of cu_seqlens; index_dtype of
+ *                     state_batch_indices, whose entry for sequence s is at
+ *                     s * sbi_stride (the row length of a 2-D table: its
+ *                     column 0, as the pages' wrapper takes).
+ *   scratch           with update_trackers: nseqs uint32 arrival counters
+ *                     (scratch_bytes >= 4 * nseqs), all ZERO before the first
+ *                     call; every completed call leaves them zero.  Unused
+ *                     (may be NULL) without update_trackers.  Two calls that
+ *                     share counters must not overlap on the device.
+ * Errors as for the other calls; rows must be below 2^31 and ring_len in
+ * [1, 2^20].
+ */
+ssu_status ssu_replay_update(const ssu_params* p, const ssu_replay_cache* rc, int64_t nseqs,
+                             int64_t rows, const void* cu_seqlens, ssu_dtype meta_dtype,
+                             const void* state_batch_indices, int64_t sbi_stride,
+                             ssu_dtype index_dtype, int update_trackers, void* scratch,
+                             int64_t scratch_bytes, struct CUstream_st* stream);
+
+/*
  * Bits of the device-side error word (values, not bit positions).
  */
 #define SSU_DEVICE_ERR_COPY_TIMEOUT 1u    /* a state tile copy never landed */
@@ -314,7 +384,7 @@ const char* ssu_status_string(ssu_status status);
 const char* ssu_last_error(void);
 
 /* ABI version of this header (bumped on any incompatible change). */
-#define SSU_ABI_VERSION 1
+#define SSU_ABI_VERSION 2
 int ssu_abi_version(void);
 
 #ifdef __cplusplus

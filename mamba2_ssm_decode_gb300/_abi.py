@@ -25,7 +25,7 @@ ALGORITHMS = {"auto": SSU_ALGO_AUTO, "direct": SSU_ALGO_DIRECT, "bulk": SSU_ALGO
 # ssu_dtype
 SSU_F32, SSU_BF16, SSU_F16, SSU_I32, SSU_I64 = 0, 1, 2, 3, 4
 
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 _c_i64 = ctypes.c_int64
 _c_int = ctypes.c_int
@@ -65,6 +65,14 @@ class SlotTable(ctypes.Structure):
                 ("step_stride", _c_i64), ("steps", _c_i64)]
 
 
+class ReplayCache(ctypes.Structure):
+    """struct ssu_replay_cache."""
+
+    _fields_ = [("x_cache", _c_p), ("B_cache", _c_p), ("dt_cache", _c_p), ("ring_len", _c_i64),
+                ("ring_start", _c_p), ("prev_num_accepted", _c_p), ("num_states", _c_i64),
+                ("logical_window", _c_i32)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -86,6 +94,10 @@ def lib() -> ctypes.CDLL:
         L.ssu_update_varlen.argtypes = [ctypes.POINTER(SSUParams), _c_i64, _c_i64, _c_p, _c_i64,
                                         _c_p, _c_int, ctypes.POINTER(SlotTable),
                                         ctypes.POINTER(SlotTable), _c_int, _c_p]
+        L.ssu_replay_update.restype = _c_int
+        L.ssu_replay_update.argtypes = [ctypes.POINTER(SSUParams), ctypes.POINTER(ReplayCache),
+                                        _c_i64, _c_i64, _c_p, _c_int, _c_p, _c_i64, _c_int, _c_int,
+                                        _c_p, _c_i64, _c_p]
         L.ssu_ring_update.restype = _c_int
         L.ssu_ring_update.argtypes = [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_i64, _c_p, _c_i64,
                                       _c_int, _c_i64, _c_int, _c_i32, _c_i32, _c_i64, _c_p]

@@ -293,6 +293,83 @@ def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
     return out
 
 
+def ssu_replay_update(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, ring_start,
+                      prev_num_accepted, logical_window, D=None, z=None, dt_bias=None,
+                      dt_softplus=False, cu_seqlens=None, state_batch_indices=None,
+                      pad_slot_id=-1, out=None, update_trackers=True, scratch=None,
+                      out_dtype=None, stream=None):
+    """ReplaySSM checkpointing update (C ABI ``ssu_replay_update``).
+
+    state [slots, H, P, N] holds checkpoints; x_cache [slots, H, R, P] and
+    B_cache [slots, G, R, N] (x dtype), dt_cache [slots, H, R] fp32 are the
+    rings; ring_start / prev_num_accepted int32 trackers by slot.  x, z
+    [rows, H, P], dt [rows, H] (per head), B, C [rows, G, N]; ``cu_seqlens``
+    [S + 1] packs several rows per sequence (None: one row per sequence).
+    ``state_batch_indices`` [S] (or [S, T]: column 0) gives each sequence's
+    slot.  With ``update_trackers`` the one-token tracker rule runs in the
+    same launch; it needs ``scratch``, S int32 counters that are zero before
+    the first call (every call leaves them zero) -- a zeroed tensor is
+    allocated when none is given.  Returns ``out``."""
+    dev = _require_cuda(state, x, dt, A, B, C, D, z, dt_bias, x_cache, B_cache, dt_cache,
+                        ring_start, prev_num_accepted, cu_seqlens, state_batch_indices, out,
+                        scratch)
+    rows = x.shape[0]
+    if dt.dim() == 3 and dt.shape[2] == 1:
+        dt = dt[:, :, 0]
+    if cu_seqlens is not None:
+        if cu_seqlens.dim() != 1 or (cu_seqlens.numel() > 1 and cu_seqlens.stride(0) != 1):
+            raise ValueError("cu_seqlens must be a contiguous vector")
+        nseqs = cu_seqlens.numel() - 1
+        meta = _int_dtype(cu_seqlens, "cu_seqlens")
+    else:
+        nseqs = rows
+        meta = _abi.SSU_I32
+    if out is None:
+        out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=dev)
+    p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out, False, rows)
+    slots, H, P, N = state.shape
+    G = B.shape[1]
+    if x_cache.dim() != 4 or tuple(x_cache.shape[:2]) != (slots, H) or x_cache.shape[3] != P:
+        raise ValueError(f"x_cache must be [{slots}, {H}, R, {P}], got {tuple(x_cache.shape)}")
+    R = x_cache.shape[2]
+    if tuple(B_cache.shape) != (slots, G, R, N):
+        raise ValueError(f"B_cache must be [{slots}, {G}, {R}, {N}], got {tuple(B_cache.shape)}")
+    if tuple(dt_cache.shape) != (slots, H, R):
+        raise ValueError(f"dt_cache must be [{slots}, {H}, {R}], got {tuple(dt_cache.shape)}")
+    for name, t, d in (("x_cache", x_cache, x.dtype), ("B_cache", B_cache, x.dtype),
+                       ("dt_cache", dt_cache, torch.float32)):
+        if t.dtype != d:
+            raise ValueError(f"{name} must be {d}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    for name, t in (("ring_start", ring_start), ("prev_num_accepted", prev_num_accepted)):
+        if t.dtype != torch.int32:
+            raise NotImplementedError(f"{name} must be int32, got {t.dtype}")
+        if t.dim() != 1 or (t.numel() > 1 and t.stride(0) != 1):
+            raise ValueError(f"{name} must be a contiguous vector")
+    sbi = state_batch_indices
+    idx = _abi.SSU_I32
+    sbi_stride = 1
+    if sbi is not None:
+        if sbi.dim() == 2:   # a [S, T] table: its column 0, as the pages' wrapper takes
+            sbi = sbi[:, 0]
+        if sbi.dim() != 1 or sbi.shape[0] != nseqs:
+            raise ValueError(f"state_batch_indices must give one slot per sequence ({nseqs})")
+        sbi_stride = sbi.stride(0)
+        idx = _int_dtype(sbi, "state_batch_indices")
+    if update_trackers and scratch is None:
+        scratch = torch.zeros(max(1, nseqs), dtype=torch.int32, device=dev)
+    rc = _abi.ReplayCache(x_cache.data_ptr(), B_cache.data_ptr(), dt_cache.data_ptr(), R,
+                          ring_start.data_ptr(), prev_num_accepted.data_ptr(),
+                          min(ring_start.numel(), prev_num_accepted.numel()),
+                          int(logical_window))
+    sb = 0 if scratch is None else scratch.numel() * scratch.element_size()
+    _abi.check(_abi.lib().ssu_replay_update(
+        ctypes.byref(p), ctypes.byref(rc), nseqs, rows, _ptr(cu_seqlens), meta, _ptr(sbi),
+        sbi_stride, idx, int(bool(update_trackers)), _ptr(scratch), sb, _stream(dev, stream)))
+    return out
+
+
 def _tracker_args(ring_start, prev_num_accepted, prev_query_len, state_batch_indices):
     for name, t in (("ring_start", ring_start), ("prev_num_accepted", prev_num_accepted),
                     ("prev_query_len", prev_query_len)):

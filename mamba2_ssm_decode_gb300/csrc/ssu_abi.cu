@@ -282,6 +282,84 @@ ssu_status ssu_update_varlen(const ssu_params* p, int64_t nseqs, int64_t rows,
   return ok();
 }
 
+ssu_status ssu_replay_update(const ssu_params* p, const ssu_replay_cache* rc, int64_t nseqs,
+                             int64_t rows, const void* cu_seqlens, ssu_dtype meta_dtype,
+                             const void* state_batch_indices, int64_t sbi_stride,
+                             ssu_dtype index_dtype, int update_trackers, void* scratch,
+                             int64_t scratch_bytes, struct CUstream_st* stream) {
+  ssu::KParams k;
+  ssu_status st = check_params(p, &k);
+  if (st != SSU_OK) return st;
+  if (p->disable_state_update)
+    return fail(SSU_ERR_UNSUPPORTED,
+                "the checkpointing update has no disable_state_update (it always caches)");
+  if (p->dt_dim_stride != 0)
+    return fail(SSU_ERR_UNSUPPORTED,
+                "the checkpointing update caches one dt per head: dt must be per head");
+  if (!rc) return fail(SSU_ERR_INVALID_ARGUMENT, "the replay cache must not be NULL");
+  if (nseqs < 0 || rows < 0) return fail(SSU_ERR_INVALID_ARGUMENT, "nseqs and rows must be >= 0");
+  if (rows > 0x7fffffffLL) return fail(SSU_ERR_UNSUPPORTED, "rows must be below 2^31");
+  if (rc->ring_len < 1 || rc->ring_len > (1 << 20))
+    return fail(SSU_ERR_INVALID_ARGUMENT, "ring_len must be in [1, 2^20], got %lld",
+                (long long)rc->ring_len);
+  if (rc->num_states < 0) return fail(SSU_ERR_INVALID_ARGUMENT, "num_states must be >= 0");
+  if (nseqs > 0 && (!rc->x_cache || !rc->B_cache || !rc->dt_cache || !rc->ring_start ||
+                    !rc->prev_num_accepted))
+    return fail(SSU_ERR_INVALID_ARGUMENT, "the ring caches and trackers must not be NULL");
+  if (state_batch_indices && !is_index(index_dtype))
+    return fail(SSU_ERR_INVALID_ARGUMENT, "state_batch_indices must be int32 or int64, got %s",
+                dtype_name(index_dtype));
+  if (cu_seqlens && !is_index(meta_dtype))
+    return fail(SSU_ERR_INVALID_ARGUMENT, "cu_seqlens must be int32 or int64, got %s",
+                dtype_name(meta_dtype));
+  if (!cu_seqlens && rows != nseqs)
+    return fail(SSU_ERR_INVALID_ARGUMENT,
+                "without cu_seqlens every sequence is one row: rows (%lld) must equal nseqs "
+                "(%lld)",
+                (long long)rows, (long long)nseqs);
+  if (!state_batch_indices && nseqs > p->slots)
+    return fail(SSU_ERR_INVALID_ARGUMENT,
+                "without state_batch_indices sequence s uses slot s: %lld sequences exceed %lld "
+                "slots",
+                (long long)nseqs, (long long)p->slots);
+  if (update_trackers &&
+      (!scratch || scratch_bytes < 4 * nseqs || reinterpret_cast<uintptr_t>(scratch) % 4 != 0))
+    return fail(SSU_ERR_INVALID_ARGUMENT,
+                "update_trackers needs 4-byte aligned scratch of 4 * nseqs = %lld bytes "
+                "(zero-filled before the first call), got %lld",
+                (long long)(4 * nseqs), (long long)scratch_bytes);
+  if (nseqs == 0) return ok();
+  ssu::ReplayArgs a{};
+  a.sbi = state_batch_indices;
+  a.sbi_stride = sbi_stride;
+  a.idx64 = index_dtype == SSU_I64;
+  a.cu = cu_seqlens;
+  a.meta64 = meta_dtype == SSU_I64;
+  a.rows = rows;
+  a.x_cache = rc->x_cache;
+  a.B_cache = rc->B_cache;
+  a.dt_cache = rc->dt_cache;
+  a.R = (int)rc->ring_len;
+  a.G = (int)p->ngroups;
+  a.W = rc->logical_window;
+  a.ring_start = rc->ring_start;
+  a.prev = rc->prev_num_accepted;
+  a.limit = rc->num_states < p->slots ? rc->num_states : p->slots;
+  a.update_trackers = update_trackers != 0;
+  a.arrivals = static_cast<unsigned*>(scratch);
+  const bool io_bf16 = p->io_dtype == SSU_BF16;
+  const int N = (int)p->dstate;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (p->state_dtype) {
+    case SSU_F32: e = ssu::replay_state_f32(N, io_bf16, k, a, nseqs, (cudaStream_t)stream); break;
+    case SSU_BF16: e = ssu::replay_state_bf16(N, io_bf16, k, a, nseqs, (cudaStream_t)stream); break;
+    case SSU_F16: e = ssu::replay_state_f16(N, io_bf16, k, a, nseqs, (cudaStream_t)stream); break;
+    default: break;
+  }
+  if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 static ssu_status check_trackers(int32_t* rs, int64_t n_rs, int32_t* pna, int64_t n_pna,
                                  int32_t* pql, int64_t n_pql, const void* sbi,
                                  ssu_dtype index_dtype, int64_t nseqs, int64_t* num_states) {

@@ -5,6 +5,7 @@
 
 #include "ssu_bulk.cuh"
 #include "ssu_headrun.cuh"
+#include "ssu_replay.cuh"
 
 namespace ssu {
 
@@ -204,6 +205,48 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
   return cudaGetLastError();
 }
 
+// ReplaySSM checkpointing update: the head-run decomposition, chains of up to
+// 8 steps staged at once (a window of 4 with 4-token passes; longer chains are
+// staged 8 steps at a time).
+constexpr int kReplayLmax = 8;
+
+template <class ST, class IT, int N>
+cudaError_t launch_replay_typed(KParams p, const ReplayArgs& ra, int64_t nseqs,
+                                cudaStream_t stream) {
+  using NT = HeadRunTune<ST, N>;
+  using RC = ReplayCfg<ST, IT, N, NT::WARPS, NT::UNR, kReplayLmax>;
+  p.tiles = (p.P + RC::ROWS - 1) / RC::ROWS;
+  set_divisors(p);
+  const int kh = heads_per_cta(p.hr, nseqs * p.H * (int64_t)p.tiles);
+  const int64_t gx = (int64_t)(p.H / kh) * p.tiles;
+  const int64_t gz = (nseqs + 65534) / 65535;
+  const int64_t gy = (nseqs + gz - 1) / gz;
+  if (gx > 0x7fffffffLL || gz > 65535) return cudaErrorInvalidConfiguration;
+  auto kern = ssu_replay_kernel<ST, IT, N, NT::WARPS, NT::UNR, kReplayLmax>;
+  const int smem = (int)sizeof(typename RC::Smem);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3((unsigned)gx, (unsigned)gy, (unsigned)gz), RC::THREADS, smem, stream>>>(p, ra, nseqs,
+                                                                                     kh);
+  return cudaGetLastError();
+}
+
+template <class ST, class IT>
+cudaError_t launch_replay_io(int N, const KParams& p, const ReplayArgs& ra, int64_t nseqs,
+                             cudaStream_t stream) {
+  switch (N) {
+    case 16: return launch_replay_typed<ST, IT, 16>(p, ra, nseqs, stream);
+    case 32: return launch_replay_typed<ST, IT, 32>(p, ra, nseqs, stream);
+    case 64: return launch_replay_typed<ST, IT, 64>(p, ra, nseqs, stream);
+    case 128: return launch_replay_typed<ST, IT, 128>(p, ra, nseqs, stream);
+    case 256: return launch_replay_typed<ST, IT, 256>(p, ra, nseqs, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
 template <class ST, class IT>
 cudaError_t launch_io(int N, bool varlen, const KParams& p, const OneTokenArgs* oa,
                       const VarlenArgs* va, int64_t nitems, cudaStream_t stream, int algo) {
@@ -227,6 +270,14 @@ cudaError_t launch_state_bf16(int N, bool io_bf16, bool varlen, const KParams& p
 cudaError_t launch_state_f16(int N, bool io_bf16, bool varlen, const KParams& p,
                              const OneTokenArgs* oa, const VarlenArgs* va, int64_t nitems,
                              cudaStream_t stream, int algorithm);
+
+// defined in ssu_state_{f32,bf16,f16}.cu
+cudaError_t replay_state_f32(int N, bool io_bf16, const KParams& p, const ReplayArgs& ra,
+                             int64_t nseqs, cudaStream_t stream);
+cudaError_t replay_state_bf16(int N, bool io_bf16, const KParams& p, const ReplayArgs& ra,
+                              int64_t nseqs, cudaStream_t stream);
+cudaError_t replay_state_f16(int N, bool io_bf16, const KParams& p, const ReplayArgs& ra,
+                             int64_t nseqs, cudaStream_t stream);
 
 // defined in selftest.cu
 cudaError_t launch_bounded_wait_probe(uint64_t limit_ns, unsigned long long* waited_ns,

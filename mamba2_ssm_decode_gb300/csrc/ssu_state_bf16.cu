@@ -10,4 +10,10 @@ cudaError_t launch_state_bf16(int N, bool io_bf16, bool varlen, const KParams& p
                  : launch_io<__nv_bfloat16, __half>(N, varlen, p, oa, va, nitems, stream, algorithm);
 }
 
+cudaError_t replay_state_bf16(int N, bool io_bf16, const KParams& p, const ReplayArgs& ra,
+                              int64_t nseqs, cudaStream_t stream) {
+  return io_bf16 ? launch_replay_io<__nv_bfloat16, __nv_bfloat16>(N, p, ra, nseqs, stream)
+                 : launch_replay_io<__nv_bfloat16, __half>(N, p, ra, nseqs, stream);
+}
+
 }  // namespace ssu

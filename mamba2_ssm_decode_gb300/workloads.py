@@ -56,6 +56,12 @@ class SSUCase:
     prev_query_len: torch.Tensor | None = None
     logical_window: int = 0
     ring_buffer_len: int = 1
+    # ReplaySSM checkpointing calls (kind "replay"): the ring caches, and whether
+    # the call applies the one-token tracker update itself
+    x_cache: torch.Tensor | None = None   # [slots, H, R, P]
+    B_cache: torch.Tensor | None = None   # [slots, G, R, N]
+    dt_cache: torch.Tensor | None = None  # [slots, H, R] fp32
+    update_trackers: bool = False
 
     @property
     def rows(self) -> int:
@@ -217,6 +223,80 @@ def varlen_case(*, nseqs, max_len, heads, headdim, dstate, groups, slots, state_
     return case
 
 
+def replay_case(*, nseqs, heads, headdim, dstate, groups, slots, state_dtype,
+                io_dtype=torch.bfloat16, max_len=1, logical_window=4, ring_len=8,
+                pad_frac=0.0, with_z=True, index_dtype=torch.int32, meta_dtype=torch.int32,
+                update_trackers=None, seed=0, device="cpu", name="replay") -> SSUCase:
+    """A ReplaySSM checkpointing call: checkpoints ~N(0, 0.1^2); ring caches
+    holding earlier tokens (x, B ~N(0, 1) in the io dtype, dt ~N(0, 1)); int32
+    trackers by slot with ring_start U{0..R-1} and, for each sequence's slot,
+    k = prev_num_accepted U{1..W} for one-token calls (the values the update
+    rule cycles through) or U{0..max(W, max_len)} after a commit, capped so the
+    ring holds k + L tokens.  max_len 1: one row per sequence (no cu_seqlens);
+    else lengths U{1..max_len} packed with cu_seqlens.  update_trackers
+    defaults to on for one-token calls, off for packed ones (their trackers
+    move by the commit)."""
+    g = _gen(seed, device)
+    one = max_len == 1
+    if one:
+        lens = torch.ones(nseqs, dtype=torch.int64, device=device)
+    else:
+        lens = torch.randint(1, max_len + 1, (nseqs,), generator=g, device=device)
+    rows = int(lens.sum().item())
+    state = _normal((slots, heads, headdim, dstate), 0.1, state_dtype, g, device)
+    x = _normal((rows, heads, headdim), 1.0, io_dtype, g, device)
+    dt = _normal((rows, heads), 1.0, torch.float32, g, device)
+    A, D, dt_bias = _head_params(heads, g, device)
+    B = _normal((rows, groups, dstate), 1.0, io_dtype, g, device)
+    C = _normal((rows, groups, dstate), 1.0, io_dtype, g, device)
+    z = _normal((rows, heads, headdim), 1.0, io_dtype, g, device) if with_z else None
+    sbi = _distinct_slots(nseqs, slots, g, device)
+    sbi = _pad_some(sbi, round(pad_frac * nseqs), PAD_SLOT_ID, g, device)
+    xc = _normal((slots, heads, ring_len, headdim), 1.0, io_dtype, g, device)
+    Bc = _normal((slots, groups, ring_len, dstate), 1.0, io_dtype, g, device)
+    dc = _normal((slots, heads, ring_len), 1.0, torch.float32, g, device)
+    rs = torch.randint(0, ring_len, (slots,), generator=g, device=device, dtype=torch.int64)
+    lo, hi = (1, logical_window) if one else (0, max(logical_window, max_len))
+    u = torch.rand((nseqs,), generator=g, device=device)
+    cap = torch.clamp(ring_len - lens, min=0)
+    k = torch.minimum(lo + torch.floor(u * (hi - lo + 1)).to(torch.int64), cap)
+    pna = torch.zeros(slots, dtype=torch.int64, device=device)
+    valid = sbi >= 0
+    pna[sbi[valid]] = k[valid]
+    cu = None
+    if not one:
+        cu = torch.zeros(nseqs + 1, dtype=torch.int64, device=device)
+        cu[1:] = torch.cumsum(lens, 0)
+        cu = cu.to(meta_dtype)
+    return SSUCase(kind="replay", name=name, state=state, x=x, dt=dt, A=A, B=B, C=C, D=D,
+                   dt_bias=dt_bias, z=z, state_batch_indices=sbi.to(index_dtype), cu_seqlens=cu,
+                   nseqs=nseqs, ring_start=rs.to(torch.int32),
+                   prev_num_accepted=pna.to(torch.int32),
+                   prev_query_len=torch.zeros(slots, dtype=torch.int32, device=device),
+                   logical_window=logical_window, ring_buffer_len=ring_len, x_cache=xc,
+                   B_cache=Bc, dt_cache=dc,
+                   update_trackers=one if update_trackers is None else update_trackers)
+
+
+def replay_decode(seed=0, device="cpu") -> SSUCase:
+    """ReplaySSM one-token decode shaped like the Mamba2-2.7B decode: batch 256,
+    80 heads, headdim 64, dstate 128, 1 group, fp32 checkpoints in a pool of
+    512 slots, 5% pad; window 4, ring 8; the tracker update in the call."""
+    return replay_case(nseqs=256, heads=80, headdim=64, dstate=128, groups=1, slots=512,
+                       state_dtype=torch.float32, pad_frac=0.05, logical_window=4, ring_len=8,
+                       seed=seed, device=device, name="replay-decode-b256")
+
+
+def replay_mtp(seed=0, device="cpu") -> SSUCase:
+    """ReplaySSM speculative pass shaped like the packed MTP workload: 128
+    sequences of U{1..4} rows, 80 heads, headdim 64, dstate 128, 1 group, fp32
+    checkpoints in a pool of 1024 slots; window 4, ring 8; trackers as left by
+    a commit (moved by ssu_ring_commit, not by the call)."""
+    return replay_case(nseqs=128, heads=80, headdim=64, dstate=128, groups=1, slots=1024,
+                       state_dtype=torch.float32, max_len=4, logical_window=4, ring_len=8,
+                       seed=seed, device=device, name="replay-mtp-s128")
+
+
 # ---------------------------------------------------------------------------
 # the named serving workloads
 # ---------------------------------------------------------------------------
@@ -305,6 +385,8 @@ WORKLOADS = {
     "mtp-varlen": mtp_varlen,
     "mamba2-2.7b-decode-perchannel": mamba2_2p7b_decode_perchannel,
     "mtp-varlen-dtperdim": mtp_varlen_dt_per_dim,
+    "replay-decode": replay_decode,
+    "replay-mtp": replay_mtp,
 }
 
 

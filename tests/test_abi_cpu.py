@@ -48,11 +48,14 @@ def test_struct_layout_matches_header(tmp_path):
     """offsetof / sizeof from a C compile of include/ssu.h equal the ctypes mirror."""
     fields = [f for f, _ in _abi.SSUParams._fields_]
     tfields = [f for f, _ in _abi.SlotTable._fields_]
+    rfields = [f for f, _ in _abi.ReplayCache._fields_]
     src = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', 'int main(void){']
     src.append('printf("%zu\\n", sizeof(ssu_params));')
     src += [f'printf("%zu\\n", offsetof(ssu_params, {f}));' for f in fields]
     src.append('printf("%zu\\n", sizeof(ssu_slot_table));')
     src += [f'printf("%zu\\n", offsetof(ssu_slot_table, {f}));' for f in tfields]
+    src.append('printf("%zu\\n", sizeof(ssu_replay_cache));')
+    src += [f'printf("%zu\\n", offsetof(ssu_replay_cache, {f}));' for f in rfields]
     src.append('printf("%zu\\n", sizeof(ssu_dtype)); return 0; }')
     c = tmp_path / "layout.c"
     c.write_text("\n".join(src))
@@ -62,6 +65,8 @@ def test_struct_layout_matches_header(tmp_path):
                                            check=True).stdout.split()]
     want = [ctypes.sizeof(_abi.SSUParams)] + [getattr(_abi.SSUParams, f).offset for f in fields]
     want += [ctypes.sizeof(_abi.SlotTable)] + [getattr(_abi.SlotTable, f).offset for f in tfields]
+    want += [ctypes.sizeof(_abi.ReplayCache)]
+    want += [getattr(_abi.ReplayCache, f).offset for f in rfields]
     want += [ctypes.sizeof(ctypes.c_int)]
     assert vals == want
 
@@ -168,6 +173,34 @@ def test_tracker_rejections(lib):
     assert com(meta=_abi.SSU_F16) == _abi.SSU_ERR_INVALID_ARGUMENT
     assert com(rb=0) == _abi.SSU_ERR_INVALID_ARGUMENT
     assert com(n=0) == _abi.SSU_OK
+
+
+def call_replay(lib, p, nseqs=2, rows=2, cu=None, meta=_abi.SSU_I32, sbi=None, idx=_abi.SSU_I32,
+                update=0, scratch=None, sbytes=0, rc=None):
+    f = FAKE
+    rc = rc or _abi.ReplayCache(f, f, f, 8, f, f, 8, 4)
+    return lib.ssu_replay_update(ctypes.byref(p), ctypes.byref(rc), nseqs, rows, cu, meta, sbi,
+                                 1, idx, update, scratch, sbytes, None)
+
+
+def test_replay_rejections(lib):
+    p = valid_params()
+    assert call_replay(lib, valid_params(disable_state_update=1)) == _abi.SSU_ERR_UNSUPPORTED
+    assert call_replay(lib, valid_params(dt_dim_stride=1)) == _abi.SSU_ERR_UNSUPPORTED
+    assert "one dt per head" in lib.ssu_last_error().decode()
+    assert call_replay(lib, p, rows=3) == _abi.SSU_ERR_INVALID_ARGUMENT     # rows != nseqs
+    assert call_replay(lib, p, nseqs=9, rows=9) == _abi.SSU_ERR_INVALID_ARGUMENT   # > slots
+    assert call_replay(lib, p, cu=FAKE, meta=_abi.SSU_F32, rows=5) == _abi.SSU_ERR_INVALID_ARGUMENT
+    assert call_replay(lib, p, sbi=FAKE, idx=_abi.SSU_BF16) == _abi.SSU_ERR_INVALID_ARGUMENT
+    bad = _abi.ReplayCache(FAKE, FAKE, FAKE, 0, FAKE, FAKE, 8, 4)
+    assert call_replay(lib, p, rc=bad) == _abi.SSU_ERR_INVALID_ARGUMENT       # ring_len 0
+    nul = _abi.ReplayCache(FAKE, None, FAKE, 8, FAKE, FAKE, 8, 4)
+    assert call_replay(lib, p, rc=nul) == _abi.SSU_ERR_INVALID_ARGUMENT
+    # the fused tracker update needs 4 * nseqs bytes of counters
+    assert call_replay(lib, p, update=1) == _abi.SSU_ERR_INVALID_ARGUMENT
+    assert "scratch" in lib.ssu_last_error().decode()
+    assert call_replay(lib, p, update=1, scratch=FAKE, sbytes=7) == _abi.SSU_ERR_INVALID_ARGUMENT
+    assert call_replay(lib, p, nseqs=0, rows=0) == _abi.SSU_OK
 
 
 def test_status_strings(lib):
