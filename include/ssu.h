@@ -347,6 +347,39 @@ ssu_status ssu_replay_update(const ssu_params* p, const ssu_replay_cache* rc, in
                              int64_t scratch_bytes, struct CUstream_st* stream);
 
 /*
+ * ssu_replay_update without a scratch argument (the pages have no counterpart
+ * of this entry point).  ssu_replay_update's tracker update counts the CTAs of
+ * each sequence in caller-provided scratch.  Some callers cannot hand the
+ * library such a buffer: a plugin host that gives an operation only its own
+ * inputs and outputs, or a serving runtime that plans all device memory at
+ * start-up and forbids allocations afterwards (a cudaMalloc can synchronise
+ * the device and break a pre-planned pool).  This entry point keeps the
+ * counters in a fixed array inside the library instead and allocates nothing:
+ * no cudaMalloc, cudaFree or allocating library routine.
+ *   - Arguments and behaviour as ssu_replay_update, without scratch.
+ *   - At most SSU_REPLAY_STATIC_MAX_SEQS sequences per call; more is rejected
+ *     (SSU_ERR_INVALID_ARGUMENT) before anything runs.  The array is 256 KB
+ *     of device memory on every GPU that loads the library, held until the
+ *     process exits.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, on the current device); make that first call before any
+ *     stream capture on the device.
+ *   - Every call on a device shares the one array and it keeps what the last
+ *     call left there: with update_trackers, each call clears the counters it
+ *     uses (an asynchronous memset on `stream`, which is issued before the
+ *     arguments are checked; the counters are the library's own, so a rejected
+ *     call still changes nothing the caller holds).  Calls whose work overlaps
+ *     on the device -- on different streams, or from different threads --
+ *     race on the counters and must not be made.
+ */
+#define SSU_REPLAY_STATIC_MAX_SEQS 65536
+ssu_status ssu_replay_update_static(const ssu_params* p, const ssu_replay_cache* rc,
+                                    int64_t nseqs, int64_t rows, const void* cu_seqlens,
+                                    ssu_dtype meta_dtype, const void* state_batch_indices,
+                                    int64_t sbi_stride, ssu_dtype index_dtype,
+                                    int update_trackers, struct CUstream_st* stream);
+
+/*
  * Bits of the device-side error word (values, not bit positions).
  */
 #define SSU_DEVICE_ERR_COPY_TIMEOUT 1u    /* a state tile copy never landed */

@@ -26,6 +26,7 @@ ALGORITHMS = {"auto": SSU_ALGO_AUTO, "direct": SSU_ALGO_DIRECT, "bulk": SSU_ALGO
 SSU_F32, SSU_BF16, SSU_F16, SSU_I32, SSU_I64 = 0, 1, 2, 3, 4
 
 ABI_VERSION = 2
+REPLAY_STATIC_MAX_SEQS = 65536   # SSU_REPLAY_STATIC_MAX_SEQS
 
 _c_i64 = ctypes.c_int64
 _c_int = ctypes.c_int
@@ -98,6 +99,10 @@ def lib() -> ctypes.CDLL:
         L.ssu_replay_update.argtypes = [ctypes.POINTER(SSUParams), ctypes.POINTER(ReplayCache),
                                         _c_i64, _c_i64, _c_p, _c_int, _c_p, _c_i64, _c_int, _c_int,
                                         _c_p, _c_i64, _c_p]
+        L.ssu_replay_update_static.restype = _c_int
+        L.ssu_replay_update_static.argtypes = [ctypes.POINTER(SSUParams),
+                                               ctypes.POINTER(ReplayCache), _c_i64, _c_i64, _c_p,
+                                               _c_int, _c_p, _c_i64, _c_int, _c_int, _c_p]
         L.ssu_ring_update.restype = _c_int
         L.ssu_ring_update.argtypes = [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_i64, _c_p, _c_i64,
                                       _c_int, _c_i64, _c_int, _c_i32, _c_i32, _c_i64, _c_p]

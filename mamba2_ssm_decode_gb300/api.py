@@ -370,6 +370,53 @@ def ssu_replay_update(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, ring_st
     return out
 
 
+def ssu_replay_update_static(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, ring_start,
+                             prev_num_accepted, logical_window, D=None, z=None, dt_bias=None,
+                             dt_softplus=False, cu_seqlens=None, state_batch_indices=None,
+                             pad_slot_id=-1, out=None, update_trackers=True, stream=None):
+    """ssu_replay_update for callers that cannot pass scratch (C ABI
+    ``ssu_replay_update_static``): the tracker counters live in a fixed array
+    inside the library, so the call needs no buffer beyond its operands.  At
+    most ``_abi.REPLAY_STATIC_MAX_SEQS`` sequences; the first call on a device
+    must come before any stream capture there; calls that overlap on the device
+    share the counters and must not be made.  ``out`` must be given (this
+    entry point is for callers that allocate nothing)."""
+    dev = _require_cuda(state, x, dt, A, B, C, D, z, dt_bias, x_cache, B_cache, dt_cache,
+                        ring_start, prev_num_accepted, cu_seqlens, state_batch_indices, out)
+    if out is None:
+        raise ValueError("ssu_replay_update_static writes into a caller-provided out")
+    rows = x.shape[0]
+    if dt.dim() == 3 and dt.shape[2] == 1:
+        dt = dt[:, :, 0]
+    nseqs, meta = rows, _abi.SSU_I32
+    if cu_seqlens is not None:
+        nseqs = cu_seqlens.numel() - 1
+        meta = _int_dtype(cu_seqlens, "cu_seqlens")
+    p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out, False, rows)
+    slots, H, P, N = state.shape
+    R = x_cache.shape[2]
+    if (tuple(x_cache.shape) != (slots, H, R, P) or tuple(B_cache.shape) != (slots, B.shape[1], R, N)
+            or tuple(dt_cache.shape) != (slots, H, R)):
+        raise ValueError("ring caches must be [slots, H, R, P], [slots, G, R, N], [slots, H, R]")
+    for t, d in ((x_cache, x.dtype), (B_cache, x.dtype), (dt_cache, torch.float32),
+                 (ring_start, torch.int32), (prev_num_accepted, torch.int32)):
+        if t.dtype != d or not t.is_contiguous():
+            raise ValueError(f"ring caches and trackers must be contiguous {d}")
+    sbi, stride, idx = state_batch_indices, 1, _abi.SSU_I32
+    if sbi is not None:
+        if sbi.dim() == 2:
+            sbi = sbi[:, 0]
+        stride, idx = sbi.stride(0), _int_dtype(sbi, "state_batch_indices")
+    rc = _abi.ReplayCache(x_cache.data_ptr(), B_cache.data_ptr(), dt_cache.data_ptr(), R,
+                          ring_start.data_ptr(), prev_num_accepted.data_ptr(),
+                          min(ring_start.numel(), prev_num_accepted.numel()),
+                          int(logical_window))
+    _abi.check(_abi.lib().ssu_replay_update_static(
+        ctypes.byref(p), ctypes.byref(rc), nseqs, rows, _ptr(cu_seqlens), meta, _ptr(sbi),
+        stride, idx, int(bool(update_trackers)), _stream(dev, stream)))
+    return out
+
+
 def _tracker_args(ring_start, prev_num_accepted, prev_query_len, state_batch_indices):
     for name, t in (("ring_start", ring_start), ("prev_num_accepted", prev_num_accepted),
                     ("prev_query_len", prev_query_len)):

@@ -73,6 +73,17 @@ ssu_status ok() {
   return SSU_OK;
 }
 
+}  // namespace
+
+namespace ssu {
+// Record a failure of an entry point defined in another translation unit.
+ssu_status record_error(ssu_status code, const char* message) {
+  return fail(code, "%s", message);
+}
+}  // namespace ssu
+
+namespace {
+
 bool is_index(ssu_dtype d) { return d == SSU_I32 || d == SSU_I64; }
 
 const char* dtype_name(ssu_dtype d) {
