@@ -229,8 +229,10 @@ cudaError_t launch_replay_typed(KParams p, const ReplayArgs& ra, int64_t nseqs,
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
+  unsigned* err = device_error_word();
+  if (!err) return cudaErrorInvalidSymbol;
   kern<<<dim3((unsigned)gx, (unsigned)gy, (unsigned)gz), RC::THREADS, smem, stream>>>(p, ra, nseqs,
-                                                                                     kh);
+                                                                                     kh, err);
   return cudaGetLastError();
 }
 

@@ -60,7 +60,7 @@ def _load():
             lib.oracle_ssu_update.argtypes = (
                 [_p, _int, _i64, _i64, _i64, _i64, _i64, _i64,
                  _p, _p, _int, _p, _int, _p, _p, _p, _p, _p, _p, _p, _i64, _int, _int, _int,
-                 _p])
+                 _p, _p, _int])
             lib.oracle_ssu_update_varlen.restype = _int
             lib.oracle_ssu_update_varlen.argtypes = (
                 [_p, _int, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
@@ -68,7 +68,7 @@ def _load():
                  _p, _i64, _p,
                  _p, _i64, _i64, _i64, _i64,
                  _p, _i64, _i64, _i64, _i64,
-                 _i64, _int, _int, _int, _p])
+                 _i64, _int, _int, _int, _p, _p, _int])
             lib.oracle_ring_update.restype = _int
             lib.oracle_ring_update.argtypes = (
                 [_p, _i64, _p, _i64, _p, _i64, _p, _i64, _i64, _int, _i32, _i32, _i64])
@@ -81,11 +81,18 @@ def _load():
                  _p, _p, _int, _p, _p, _p, _p, _p, _p,
                  _p, _p, _i64,
                  _p, _p, _p, _i64,
-                 _p, _p, _i64, _i32, _int, _int, _int, _p])
+                 _p, _p, _i64, _i32, _int, _int, _int, _p, _p, _int])
             lib.oracle_replay_state.restype = _int
             lib.oracle_replay_state.argtypes = (
                 [_p, _int, _i64, _i64, _i64, _i64, _i64, _int, _p, _p, _int, _int,
                  _i64, _p, _p, _p, _i64, _p, _p, _i64, _p])
+            lib.oracle_philox4x64.restype = None
+            lib.oracle_philox4x64.argtypes = [_p, _p, _int, _p]
+            lib.oracle_sr_bits.restype = ctypes.c_uint32
+            lib.oracle_sr_bits.argtypes = [ctypes.c_uint64, _int, _i64]
+            for f in ("oracle_sr_bf16", "oracle_sr_f16"):
+                getattr(lib, f).restype = ctypes.c_double
+                getattr(lib, f).argtypes = [ctypes.c_double, ctypes.c_uint32]
             lib.oracle_encode.restype = None
             lib.oracle_encode.argtypes = [_p, _i64, _int, _p]
             lib.oracle_decode.restype = None
@@ -99,6 +106,19 @@ def _load():
 
 def _ptr(t: torch.Tensor | None):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _seed(rand_seed):
+    """(pointer, keep-alive box) of the call's 64-bit random seed (stochastic
+    rounding of 16-bit state), or (None, None)."""
+    if rand_seed is None:
+        return None, None
+    if isinstance(rand_seed, torch.Tensor):
+        v = int(rand_seed.reshape(-1)[0].item())
+    else:
+        v = int(rand_seed)
+    box = ctypes.c_uint64(v % (1 << 64))
+    return ctypes.byref(box), box
 
 
 def _cpu(t, dtype=None):
@@ -143,7 +163,7 @@ def _check_io(x, z, B, C):
 
 def ssu_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
                state_batch_indices=None, dst_state_batch_indices=None, pad_slot_id=-1,
-               disable_state_update=False):
+               disable_state_update=False, rand_seed=None, philox_rounds=10):
     """One-token decode on CPU tensors.
 
     state: [slots, H, P, N] CPU tensor, updated IN PLACE (must be contiguous).
@@ -164,11 +184,12 @@ def ssu_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=
     sbi = _cpu(state_batch_indices, torch.int64)
     dsbi = _cpu(dst_state_batch_indices, torch.int64)
     y = torch.empty((batch, H, P), dtype=torch.float64)
+    seed, _box = _seed(rand_seed)
     rc = lib.oracle_ssu_update(
         _ptr(state), _DT[state.dtype], slots, H, P, N, G, batch,
         _ptr(x), _ptr(z), io, _ptr(dt), dt_per_dim, _ptr(A), _ptr(D), _ptr(dt_bias),
         _ptr(B), _ptr(C), _ptr(sbi), _ptr(dsbi), int(pad_slot_id), int(bool(dt_softplus)),
-        int(bool(disable_state_update)), per_dim, _ptr(y))
+        int(bool(disable_state_update)), per_dim, _ptr(y), seed, int(philox_rounds))
     if rc != 0:
         raise ValueError(f"oracle_ssu_update rejected its arguments (code {rc})")
     return y
@@ -190,7 +211,8 @@ def _table(t):
 def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
                       cu_seqlens=None, nseqs=None, dense_steps=1, num_accepted_tokens=None,
                       state_batch_indices=None, dst_state_batch_indices=None, pad_slot_id=-1,
-                      disable_state_update=False, src_table=None, dst_table=None):
+                      disable_state_update=False, src_table=None, dst_table=None,
+                      rand_seed=None, philox_rounds=10):
     """Packed varlen / MTP update on CPU tensors.
 
     x, z: [rows, H, P]; dt: [rows, H] or [rows, H, P]; B, C: [rows, G, N].
@@ -221,6 +243,7 @@ def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
     src = (_cpu(src[0], torch.int64),) + tuple(src[1:]) if src[0] is not None else src
     dst = (_cpu(dst[0], torch.int64),) + tuple(dst[1:]) if dst[0] is not None else dst
     y = torch.full((rows, H, P), float("nan"), dtype=torch.float64)
+    seed, _box = _seed(rand_seed)
     rc = lib.oracle_ssu_update_varlen(
         _ptr(state), _DT[state.dtype], slots, H, P, N, G, nseqs, rows,
         _ptr(x), _ptr(z), io, _ptr(dt), dt_per_dim, _ptr(A), _ptr(D), _ptr(dt_bias),
@@ -228,7 +251,7 @@ def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
         _ptr(src[0]), src[1], src[2], src[3], src[4],
         _ptr(dst[0]), dst[1], dst[2], dst[3], dst[4],
         int(pad_slot_id), int(bool(dt_softplus)), int(bool(disable_state_update)), per_dim,
-        _ptr(y))
+        _ptr(y), seed, int(philox_rounds))
     if rc != 0:
         raise ValueError(f"oracle_ssu_update_varlen rejected its arguments (code {rc})")
     return y
@@ -292,7 +315,7 @@ def _replay_caches(x_cache, B_cache, dt_cache, ring_start, prev_num_accepted, io
 def replay_update(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, ring_start,
                   prev_num_accepted, logical_window, D=None, z=None, dt_bias=None,
                   dt_softplus=False, cu_seqlens=None, state_batch_indices=None, pad_slot_id=-1,
-                  update_trackers=True, nseqs=None):
+                  update_trackers=True, nseqs=None, rand_seed=None, philox_rounds=10):
     """ReplaySSM checkpointing update on CPU tensors (ssu_oracle.c,
     oracle_replay_update: the readings are stated there).
 
@@ -324,13 +347,15 @@ def replay_update(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, ring_start,
     if sbi is not None:
         sbi = sbi.reshape(sbi.shape[0], -1)[:, 0].contiguous()   # column 0 of a 2-D table
     y = torch.full((rows, H, P), float("nan"), dtype=torch.float64)
+    seed, _box = _seed(rand_seed)
     rc = lib.oracle_replay_update(
         _ptr(state), _DT[state.dtype], slots, H, P, N, G, nseqs, rows,
         _ptr(x), _ptr(z), io, _ptr(dt), _ptr(A), _ptr(D), _ptr(dt_bias), _ptr(B), _ptr(C),
         _ptr(cu), _ptr(sbi), int(pad_slot_id),
         _ptr(x_cache), _ptr(B_cache), _ptr(dt_cache), R,
         _ptr(ring_start), _ptr(prev_num_accepted), num_states, int(logical_window),
-        int(bool(update_trackers)), int(bool(dt_softplus)), per_dim, _ptr(y))
+        int(bool(update_trackers)), int(bool(dt_softplus)), per_dim, _ptr(y), seed,
+        int(philox_rounds))
     if rc != 0:
         raise ValueError(f"oracle_replay_update rejected its arguments (code {rc})")
     return y
@@ -355,6 +380,28 @@ def replay_state(state, slot, A, x_cache, B_cache, dt_cache, ring_start, prev_nu
     if rc != 0:
         raise ValueError(f"oracle_replay_state: slot {slot} has out-of-range trackers")
     return out
+
+
+def philox4x64(counter, key, rounds=10):
+    """Philox4x64 of a 4-word counter and a 2-word key (python ints) -> 4 ints."""
+    lib = _load()
+    c = (ctypes.c_uint64 * 4)(*[int(v) % (1 << 64) for v in counter])
+    k = (ctypes.c_uint64 * 2)(*[int(v) % (1 << 64) for v in key])
+    out = (ctypes.c_uint64 * 4)()
+    lib.oracle_philox4x64(c, k, int(rounds), out)
+    return list(out)
+
+
+def sr_bits(seed, e, rounds=10):
+    """The 16 random bits of stored element e (index in the state pool) under `seed`."""
+    return int(_load().oracle_sr_bits(int(seed) % (1 << 64), int(rounds), int(e)))
+
+
+def sr_round(v, dtype, r):
+    """Stochastic rounding of the double v to bf16 / fp16 with random bits r."""
+    lib = _load()
+    f = {torch.bfloat16: lib.oracle_sr_bf16, torch.float16: lib.oracle_sr_f16}[dtype]
+    return f(float(v), int(r))
 
 
 def round_to(values: torch.Tensor, dtype: torch.dtype) -> torch.Tensor:

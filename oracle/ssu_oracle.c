@@ -158,6 +158,108 @@ static void store_rounded(void* base, int64_t i, int dtype, double v) {
   }
 }
 
+/* ------------------------------------------------------------------------ */
+/* stochastic rounding of 16-bit state                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Philox4x64 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+ * as 1, 2, 3", SC'11): a counter of four 64-bit words and a key of two are
+ * mixed by `rounds` rounds; a round multiplies words 0 and 2 by two fixed
+ * 64-bit constants, takes the 128-bit products' high and low halves, xors
+ * the high halves with the other two words and the key, and permutes; the
+ * key advances by two fixed Weyl increments between rounds.  ("ssu_dispatch"
+ * names the generator -- philox_rounds, default 10 -- and a random seed drawn
+ * per call, not the variant or the counter layout: both are readings.)
+ */
+static void mul128(uint64_t a, uint64_t b, uint64_t* hi, uint64_t* lo) {
+  /* schoolbook product of 32-bit halves: exact in 64-bit arithmetic */
+  const uint64_t a0 = a & 0xffffffffu, a1 = a >> 32, b0 = b & 0xffffffffu, b1 = b >> 32;
+  const uint64_t p00 = a0 * b0, p01 = a0 * b1, p10 = a1 * b0, p11 = a1 * b1;
+  const uint64_t mid = (p00 >> 32) + (p01 & 0xffffffffu) + (p10 & 0xffffffffu);
+  *lo = (mid << 32) | (p00 & 0xffffffffu);
+  *hi = p11 + (p01 >> 32) + (p10 >> 32) + (mid >> 32);
+}
+
+void oracle_philox4x64(const uint64_t* counter, const uint64_t* key, int rounds,
+                       uint64_t* out) {
+  uint64_t x0 = counter[0], x1 = counter[1], x2 = counter[2], x3 = counter[3];
+  uint64_t k0 = key[0], k1 = key[1];
+  for (int i = 0; i < rounds; ++i) {
+    uint64_t hi0, lo0, hi1, lo1;
+    mul128(0xD2E7470EE14C6C93ull, x0, &hi0, &lo0);
+    mul128(0xCA5A826395121157ull, x2, &hi1, &lo1);
+    const uint64_t n0 = hi1 ^ x1 ^ k0, n1 = lo1, n2 = hi0 ^ x3 ^ k1, n3 = lo0;
+    x0 = n0;
+    x1 = n1;
+    x2 = n2;
+    x3 = n3;
+    k0 += 0x9E3779B97F4A7C15ull; /* Weyl increments: golden ratio, sqrt(3) - 1 */
+    k1 += 0xBB67AE8584CAA73Bull;
+  }
+  out[0] = x0;
+  out[1] = x1;
+  out[2] = x2;
+  out[3] = x3;
+}
+
+/* The 16 random bits of stored element e (its index in the state pool) of a
+ * call with `seed`: block e / 16 of the stream keyed by (seed, 0), word
+ * (e / 4) mod 4 of it, bits 16 (e mod 4) .. 16 (e mod 4) + 15. */
+uint32_t oracle_sr_bits(uint64_t seed, int rounds, int64_t e) {
+  const uint64_t counter[4] = {(uint64_t)e >> 4, 0, 0, 0}, key[2] = {seed, 0};
+  uint64_t out[4];
+  oracle_philox4x64(counter, key, rounds, out);
+  return (uint32_t)((out[((uint64_t)e >> 2) & 3] >> (16 * ((uint64_t)e & 3))) & 0xffffu);
+}
+
+/* Stochastic rounding of v to a binary format of `prec` significant bits and
+ * minimum normal exponent `emin`: with q the format's spacing at |v| and
+ * a = |v| / q, the result is q floor(a + r / 2^16) -- the upper neighbour
+ * exactly when frac(a) >= 1 - r / 2^16, i.e. with probability frac(a) to 16
+ * bits.  Representable values are unchanged; beyond the largest finite value
+ * the result is infinite, as rounding makes it. */
+static double sr_to_precision(double v, int prec, int emin, double maxfinite, uint32_t r) {
+  if (v == 0.0 || isnan(v) || isinf(v)) return v;
+  int e;
+  (void)frexp(fabs(v), &e);
+  int E = e - 1;
+  if (E < emin) E = emin;
+  const double q = ldexp(1.0, E - (prec - 1));
+  const double a = fabs(v) / q; /* exact: a power-of-two scaling */
+  const double fl = floor(a);
+  const double frac = a - fl; /* exact */
+  double t = fl + (frac >= 1.0 - ldexp((double)r, -16) ? 1.0 : 0.0);
+  double m = t * q;
+  if (m > maxfinite) m = INFINITY;
+  return copysign(m, v);
+}
+
+double oracle_sr_bf16(double v, uint32_t r) {
+  return sr_to_precision(v, 8, -126, ldexp(255.0, 120), r);
+}
+
+double oracle_sr_f16(double v, uint32_t r) { return sr_to_precision(v, 11, -14, 65504.0, r); }
+
+/* Stochastic rounding of state writes: a call's random seed (NULL: round to
+ * nearest even) and Philox rounds; only 16-bit state is affected. */
+typedef struct {
+  const uint64_t* seed;
+  int rounds;
+} sr_ctx;
+
+static void store_state(void* base, int64_t i, int dtype, double v, const sr_ctx* sr) {
+  if (!sr || !sr->seed || (dtype != OR_BF16 && dtype != OR_F16)) {
+    store_rounded(base, i, dtype, v);
+    return;
+  }
+  const uint32_t r = oracle_sr_bits(*sr->seed, sr->rounds, i);
+  if (dtype == OR_BF16)
+    ((uint16_t*)base)[i] = exact_double_to_bf16_bits(oracle_sr_bf16(v, r));
+  else
+    ((uint16_t*)base)[i] = exact_double_to_f16_bits(oracle_sr_f16(v, r));
+}
+
 /* Round an array of doubles to `dtype` and write the stored encoding. */
 void oracle_encode(const double* v, int64_t n, int dtype, void* out) {
   for (int64_t i = 0; i < n; ++i) store_rounded(out, i, dtype, v[i]);
@@ -239,10 +341,12 @@ int oracle_ssu_update(void* state, int state_dtype, int64_t slots,
                       const float* A, const float* D, const float* dt_bias,
                       const void* B, const void* C,
                       const int64_t* sbi, const int64_t* dsbi, int64_t pad_slot_id,
-                      int dt_softplus, int disable_state_update, int param_per_dim, double* y) {
+                      int dt_softplus, int disable_state_update, int param_per_dim, double* y,
+                      const uint64_t* rand_seed, int philox_rounds) {
   if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0) return 1;
   operands o = {H, P, N, G, x, z, io_dtype, dt, dt_per_dim, A, D, dt_bias, B, C, dt_softplus,
                 param_per_dim};
+  const sr_ctx sr = {rand_seed, philox_rounds};
   const int64_t block = P * N;
   double* hb = (double*)malloc(sizeof(double) * (size_t)block);
   if (!hb) return 2;
@@ -258,7 +362,7 @@ int oracle_ssu_update(void* state, int state_dtype, int64_t slots,
       ssu_step(&o, b, h, hb, y);
       if (write_ok) {
         const int64_t out_off = (dst * H + h) * block;
-        for (int64_t i = 0; i < block; ++i) store_rounded(state, out_off + i, state_dtype, hb[i]);
+        for (int64_t i = 0; i < block; ++i) store_state(state, out_off + i, state_dtype, hb[i], &sr);
       }
     }
   }
@@ -307,10 +411,12 @@ int oracle_ssu_update_varlen(void* state, int state_dtype, int64_t slots,
                              const int64_t* dst_tab, int64_t dst_numel, int64_t dst_ss,
                              int64_t dst_ts, int64_t dst_steps,
                              int64_t pad_slot_id, int dt_softplus, int disable_state_update,
-                             int param_per_dim, double* y) {
+                             int param_per_dim, double* y, const uint64_t* rand_seed,
+                             int philox_rounds) {
   if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0) return 1;
   operands o = {H, P, N, G, x, z, io_dtype, dt, dt_per_dim, A, D, dt_bias, B, C, dt_softplus,
                 param_per_dim};
+  const sr_ctx sr = {rand_seed, philox_rounds};
   const int64_t block = P * N;
   double* hb = (double*)malloc(sizeof(double) * (size_t)block);
   if (!hb) return 2;
@@ -346,7 +452,7 @@ int oracle_ssu_update_varlen(void* state, int state_dtype, int64_t slots,
           have = table_entry(src_tab, src_numel, src_ss, src_ts, src_steps, s, t, &dst) == 0;
         if (!have || !slot_ok(dst, pad_slot_id, slots)) continue;
         const int64_t out_off = (dst * H + h) * block;
-        for (int64_t i = 0; i < block; ++i) store_rounded(state, out_off + i, state_dtype, hb[i]);
+        for (int64_t i = 0; i < block; ++i) store_state(state, out_off + i, state_dtype, hb[i], &sr);
       }
     }
   }
@@ -519,10 +625,12 @@ int oracle_replay_update(void* state, int state_dtype, int64_t slots,
                          void* x_cache, void* B_cache, float* dt_cache, int64_t ring_len,
                          int32_t* ring_start, int32_t* prev_num_accepted, int64_t num_states,
                          int32_t logical_window, int update_trackers, int dt_softplus,
-                         int param_per_dim, double* y) {
+                         int param_per_dim, double* y, const uint64_t* rand_seed,
+                         int philox_rounds) {
   if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0 || ring_len < 1) return 1;
   operands o = {H, P, N, G, x, z, io_dtype, dt, 0, A, D, dt_bias, B, C, dt_softplus,
                 param_per_dim};
+  const sr_ctx sr = {rand_seed, philox_rounds};
   const int64_t block = P * N;
   const int64_t limit = slots < num_states ? slots : num_states;
   double* hb = (double*)malloc(sizeof(double) * (size_t)block);
@@ -554,7 +662,7 @@ int oracle_replay_update(void* state, int state_dtype, int64_t slots,
           replay_token(&o, h, x_cache, B_cache, dt_cache, slot, ((int64_t)start + j) % ring_len,
                        ring_len, xrow, Brow, dtrow, ydump, hb);
         if (checkpoint)
-          for (int64_t i = 0; i < block; ++i) store_rounded(state, off + i, state_dtype, hb[i]);
+          for (int64_t i = 0; i < block; ++i) store_state(state, off + i, state_dtype, hb[i], &sr);
       }
       for (int64_t t = 0; t < L; ++t) {
         const int64_t r = begin + t;

@@ -54,6 +54,17 @@ MUTANTS = {
     "replay_B_of_first_group": ("B, (r * G + g) * N + n,", "B, (r * G + 0) * N + n,"),
     "replay_trackers_for_unprocessed": ("      if (!processed[s]) continue;\n",
                                         "      (void)processed;\n"),
+    # stochastic rounding
+    "sr_threshold_strict": ("frac >= 1.0 - ldexp((double)r, -16)",
+                            "frac > 1.0 - ldexp((double)r, -16)"),
+    "sr_counter_per_element": ("const uint64_t counter[4] = {(uint64_t)e >> 4, 0, 0, 0}",
+                               "const uint64_t counter[4] = {(uint64_t)e, 0, 0, 0}"),
+    "sr_word_from_low_bits": ("out[((uint64_t)e >> 2) & 3]", "out[(uint64_t)e & 3]"),
+    "philox_weyl_swapped": ("k0 += 0x9E3779B97F4A7C15ull;", "k0 += 0xBB67AE8584CAA73Bull;"),
+    "philox_halves_swapped": ("const uint64_t n0 = hi1 ^ x1 ^ k0, n1 = lo1, n2 = hi0 ^ x3 ^ k1, n3 = lo0;",
+                              "const uint64_t n0 = lo1 ^ x1 ^ k0, n1 = hi1, n2 = hi0 ^ x3 ^ k1, n3 = lo0;"),
+    "sr_ignored_in_state_writes": ("if (!sr || !sr->seed || (dtype != OR_BF16",
+                                   "if (1 || !sr || !sr->seed || (dtype != OR_BF16"),
 }
 
 
@@ -71,6 +82,7 @@ def test_pins_catch_mutant(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
                         os.path.join(ROOT, "tests", "test_oracle_trackers.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_replay.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_replay.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_sr.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
