@@ -130,6 +130,18 @@ typedef enum ssu_dtype {
  * pad_slot_id: slot id that marks a padded entry (vLLM passes its null
  *            block id; "mate.mamba" defaults to -1).
  * algorithm  an ssu_algorithm (0 = auto).
+ * rand_seed  NULL: state is stored rounded to nearest even.  Otherwise a
+ *            DEVICE pointer to this call's 64-bit random seed ("ssu_dispatch":
+ *            rand_seed drawn per call when stochastic rounding is enabled),
+ *            8-byte aligned: every value stored into a bf16 / fp16 pool is
+ *            rounded stochastically -- away from zero with probability equal
+ *            to its fraction between the format's two neighbours, to 16
+ *            bits.  Stored element e (its index in the pool) takes the 16 bits
+ *            16 (e mod 4) .. 16 (e mod 4) + 15 of word (e / 4) mod 4 of the
+ *            Philox4x64 block with counter (e / 16, 0, 0, 0) and key
+ *            (seed, 0).  fp32 pools ignore it.
+ * philox_rounds  Philox rounds; <= 0 means 10 ("ssu_dispatch":
+ *            philox_rounds ... or 10).
  */
 typedef struct ssu_params {
   void* state;
@@ -159,6 +171,8 @@ typedef struct ssu_params {
   int disable_state_update;
   int64_t pad_slot_id;
   int algorithm; /* ssu_algorithm */
+  const uint64_t* rand_seed;
+  int philox_rounds;
 } ssu_params;
 
 /*
@@ -417,7 +431,7 @@ const char* ssu_status_string(ssu_status status);
 const char* ssu_last_error(void);
 
 /* ABI version of this header (bumped on any incompatible change). */
-#define SSU_ABI_VERSION 2
+#define SSU_ABI_VERSION 3
 int ssu_abi_version(void);
 
 #ifdef __cplusplus

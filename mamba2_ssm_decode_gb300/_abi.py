@@ -25,7 +25,7 @@ ALGORITHMS = {"auto": SSU_ALGO_AUTO, "direct": SSU_ALGO_DIRECT, "bulk": SSU_ALGO
 # ssu_dtype
 SSU_F32, SSU_BF16, SSU_F16, SSU_I32, SSU_I64 = 0, 1, 2, 3, 4
 
-ABI_VERSION = 2
+ABI_VERSION = 3
 REPLAY_STATIC_MAX_SEQS = 65536   # SSU_REPLAY_STATIC_MAX_SEQS
 
 _c_i64 = ctypes.c_int64
@@ -56,6 +56,7 @@ class SSUParams(ctypes.Structure):
         ("dt_softplus", _c_int), ("disable_state_update", _c_int),
         ("pad_slot_id", _c_i64),
         ("algorithm", _c_int),
+        ("rand_seed", _c_p), ("philox_rounds", _c_int),
     ]
 
 

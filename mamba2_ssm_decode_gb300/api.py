@@ -93,8 +93,20 @@ def _per_head(t, heads, dim, name):
         f"with strides {t.stride()}")
 
 
+def _seed_ptr(rand_seed, dev):
+    """Device address of the call's 64-bit seed (a CUDA int64 / uint64 tensor of
+    one element, as the pages draw it), or None."""
+    if rand_seed is None:
+        return None
+    if not rand_seed.is_cuda or rand_seed.device != dev:
+        raise ValueError("rand_seed must be a one-element tensor on the call's device")
+    if rand_seed.dtype not in (torch.int64, torch.uint64) or rand_seed.numel() != 1:
+        raise ValueError("rand_seed must be one 64-bit integer")
+    return rand_seed.data_ptr()
+
+
 def _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
-            disable_state_update, rows, algorithm="auto"):
+            disable_state_update, rows, algorithm="auto", rand_seed=None, philox_rounds=10):
     if state.dim() != 4:
         raise ValueError(f"state must be [slots, heads, dim, dstate], got {tuple(state.shape)}")
     if not state.is_contiguous():
@@ -152,27 +164,31 @@ def _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
     if algorithm not in _abi.ALGORITHMS:
         raise ValueError(f"algorithm must be one of {sorted(_abi.ALGORITHMS)}, got {algorithm!r}")
     p.algorithm = _abi.ALGORITHMS[algorithm]
+    p.rand_seed = _seed_ptr(rand_seed, state.device)
+    p.philox_rounds = int(philox_rounds or 10)
     return p
 
 
 def ssu_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
                state_batch_indices=None, dst_state_batch_indices=None, pad_slot_id=-1,
                out=None, disable_state_update=False, out_dtype=None, algorithm="auto",
-               stream=None):
+               stream=None, rand_seed=None, philox_rounds=10):
     """One-token selective state update (C ABI ``ssu_update``).
 
     state [slots, H, P, N] (updated in place); x, z [batch, H, P]; dt [batch, H]
     or [batch, H, P] fp32; B, C [batch, G, N]; A, D, dt_bias per head fp32;
     slot vectors [batch] int32/int64.  Returns ``out`` [batch, H, P] (x dtype,
     or ``out_dtype=torch.float32``).  ``algorithm``: "auto", "direct" or "bulk"
-    (the two kernels of the library; identical results)."""
+    (the two kernels of the library; identical results).  ``rand_seed``: a
+    one-element int64 CUDA tensor turns on stochastic rounding of a 16-bit
+    state pool (``philox_rounds`` Philox rounds)."""
     dev = _require_cuda(state, x, dt, A, B, C, D, z, dt_bias, state_batch_indices,
-                        dst_state_batch_indices, out)
+                        dst_state_batch_indices, out, rand_seed)
     batch = x.shape[0]
     if out is None:
         out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=dev)
     p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
-                disable_state_update, batch, algorithm)
+                disable_state_update, batch, algorithm, rand_seed, philox_rounds)
     idx_dt = 0
     for name, t in (("state_batch_indices", state_batch_indices),
                     ("dst_state_batch_indices", dst_state_batch_indices)):
@@ -210,15 +226,16 @@ def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
                       cu_seqlens=None, num_accepted_tokens=None, state_batch_indices=None,
                       dst_state_batch_indices=None, pad_slot_id=-1, out=None,
                       disable_state_update=False, nseqs=None, out_dtype=None, algorithm="auto",
-                      stream=None):
+                      stream=None, rand_seed=None, philox_rounds=10):
     """Packed varlen / MTP selective state update (C ABI ``ssu_update_varlen``).
 
     x is packed [rows, H, P] with ``cu_seqlens`` [S + 1], or dense
     [batch, steps, H, P] (then dt/B/C/z are 4-D as well and equal-length
     sequences are implied).  Slot tables are [S, T] or flat [rows];
-    ``num_accepted_tokens`` [S] picks the read position (count - 1)."""
+    ``num_accepted_tokens`` [S] picks the read position (count - 1).
+    ``rand_seed`` / ``philox_rounds``: stochastic rounding, as for ssu_update."""
     dev = _require_cuda(state, x, dt, A, B, C, D, z, dt_bias, cu_seqlens, num_accepted_tokens,
-                        state_batch_indices, dst_state_batch_indices, out)
+                        state_batch_indices, dst_state_batch_indices, out, rand_seed)
     dense_steps = 1
     dense_out = None
     dense_shape = None
@@ -259,7 +276,7 @@ def ssu_update_varlen(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
     if out is None:
         out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=dev)
     p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
-                disable_state_update, rows, algorithm)
+                disable_state_update, rows, algorithm, rand_seed, philox_rounds)
     meta_dt = 0
     if cu_seqlens is not None:
         if cu_seqlens.dim() != 1 or cu_seqlens.numel() != nseqs + 1:
@@ -297,7 +314,7 @@ def ssu_replay_update(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, ring_st
                       prev_num_accepted, logical_window, D=None, z=None, dt_bias=None,
                       dt_softplus=False, cu_seqlens=None, state_batch_indices=None,
                       pad_slot_id=-1, out=None, update_trackers=True, scratch=None,
-                      out_dtype=None, stream=None):
+                      out_dtype=None, stream=None, rand_seed=None, philox_rounds=10):
     """ReplaySSM checkpointing update (C ABI ``ssu_replay_update``).
 
     state [slots, H, P, N] holds checkpoints; x_cache [slots, H, R, P] and
@@ -309,10 +326,12 @@ def ssu_replay_update(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, ring_st
     slot.  With ``update_trackers`` the one-token tracker rule runs in the
     same launch; it needs ``scratch``, S int32 counters that are zero before
     the first call (every call leaves them zero) -- a zeroed tensor is
-    allocated when none is given.  Returns ``out``."""
+    allocated when none is given.  ``rand_seed`` / ``philox_rounds``:
+    stochastic rounding of 16-bit checkpoints, as for ssu_update.  Returns
+    ``out``."""
     dev = _require_cuda(state, x, dt, A, B, C, D, z, dt_bias, x_cache, B_cache, dt_cache,
                         ring_start, prev_num_accepted, cu_seqlens, state_batch_indices, out,
-                        scratch)
+                        scratch, rand_seed)
     rows = x.shape[0]
     if dt.dim() == 3 and dt.shape[2] == 1:
         dt = dt[:, :, 0]
@@ -326,7 +345,8 @@ def ssu_replay_update(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, ring_st
         meta = _abi.SSU_I32
     if out is None:
         out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=dev)
-    p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out, False, rows)
+    p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out, False, rows,
+                "auto", rand_seed, philox_rounds)
     slots, H, P, N = state.shape
     G = B.shape[1]
     if x_cache.dim() != 4 or tuple(x_cache.shape[:2]) != (slots, H) or x_cache.shape[3] != P:
@@ -373,7 +393,8 @@ def ssu_replay_update(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, ring_st
 def ssu_replay_update_static(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, ring_start,
                              prev_num_accepted, logical_window, D=None, z=None, dt_bias=None,
                              dt_softplus=False, cu_seqlens=None, state_batch_indices=None,
-                             pad_slot_id=-1, out=None, update_trackers=True, stream=None):
+                             pad_slot_id=-1, out=None, update_trackers=True, stream=None,
+                             rand_seed=None, philox_rounds=10):
     """ssu_replay_update for callers that cannot pass scratch (C ABI
     ``ssu_replay_update_static``): the tracker counters live in a fixed array
     inside the library, so the call needs no buffer beyond its operands.  At
@@ -392,7 +413,8 @@ def ssu_replay_update_static(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, 
     if cu_seqlens is not None:
         nseqs = cu_seqlens.numel() - 1
         meta = _int_dtype(cu_seqlens, "cu_seqlens")
-    p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out, False, rows)
+    p = _params(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out, False, rows,
+                "auto", rand_seed, philox_rounds)
     slots, H, P, N = state.shape
     R = x_cache.shape[2]
     if (tuple(x_cache.shape) != (slots, H, R, P) or tuple(B_cache.shape) != (slots, B.shape[1], R, N)

@@ -186,6 +186,13 @@ ssu_status check_params(const ssu_params* p, ssu::KParams* k) {
   k->softplus = p->dt_softplus != 0;
   k->disable = p->disable_state_update != 0;
   k->pad = p->pad_slot_id;
+  if (reinterpret_cast<uintptr_t>(p->rand_seed) % 8 != 0)
+    return fail(SSU_ERR_INVALID_ARGUMENT, "rand_seed must be 8-byte aligned");
+  if (p->philox_rounds > 64)
+    return fail(SSU_ERR_INVALID_ARGUMENT, "philox_rounds must be at most 64, got %d",
+                p->philox_rounds);
+  k->sr_seed = reinterpret_cast<const unsigned long long*>(p->rand_seed);
+  k->sr_rounds = p->philox_rounds > 0 ? p->philox_rounds : 10;
   return SSU_OK;
 }
 

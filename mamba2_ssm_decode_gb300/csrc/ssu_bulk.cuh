@@ -570,8 +570,8 @@ __global__ void __launch_bounds__(WARPS * 32 + 32,
             if (prow < p.P) {
 #pragma unroll
               for (int c = 0; c < L::CPL; ++c)
-                st_state(base + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
-                         Elem<ST>::pack2(&hs[u][c * L::VEC / 2]));
+                store_state<ST>(state, base - state + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
+                                &hs[u][c * L::VEC / 2], p);
             }
           }
         }
@@ -820,8 +820,8 @@ __global__ void __launch_bounds__(WARPS * 32 + 32)
             if (prow < p.P) {
 #pragma unroll
               for (int c = 0; c < L::CPL; ++c)
-                st_state(base + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
-                         Elem<ST>::pack2(&hs[u][c * L::VEC / 2]));
+                store_state<ST>(state, base - state + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
+                                &hs[u][c * L::VEC / 2], p);
             }
           }
         }

@@ -900,8 +900,8 @@ __global__ void __launch_bounds__(WARPS * 32, sizeof(ST) == 2 ? 3 : 16 / WARPS)
           if (prow < p.P) {
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c)
-              st_state(base + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
-                       Elem<ST>::pack2(&hs[u][c * L::VEC / 2]));
+              store_state<ST>(state, base - state + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
+                              &hs[u][c * L::VEC / 2], p);
           }
         }
       }

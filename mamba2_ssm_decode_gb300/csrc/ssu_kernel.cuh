@@ -31,6 +31,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace ssu {
 
 // Exact n / d for 0 <= n < 2^31 and 1 <= d < 2^31 by one high multiply, an
@@ -85,6 +87,8 @@ struct KParams {
   int xz_vec16;  // so do x and z rows, and headdim is a multiple of 8
   int64_t pad;
   FastDiv fd_tiles, fd_H, fd_hr;  // divisions by tiles, H and heads per group
+  const unsigned long long* sr_seed;  // stochastic rounding of 16-bit state: the call's seed
+  int sr_rounds;                      // Philox rounds (used when sr_seed is set)
 };
 
 // (sequence, head, tile) of work index `idx` (< 2^31), tile fastest.
@@ -363,6 +367,108 @@ __device__ __forceinline__ void st_state(void* p, const uint4& v) {
 }
 
 // ---------------------------------------------------------------------------
+// stochastic rounding of 16-bit state
+// ---------------------------------------------------------------------------
+
+// Philox4x64 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+// 1, 2, 3", SC'11): per round, words 0 and 2 are multiplied by two fixed
+// 64-bit constants; the products' high halves are xored with words 1, 3 and
+// the key, low halves become words 1, 3; the key advances by two Weyl
+// increments.
+__device__ __forceinline__ void philox4x64(uint64_t (&x)[4], uint64_t k0, uint64_t k1,
+                                           int rounds) {
+  constexpr uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+#pragma unroll 1
+  for (int i = 0; i < rounds; ++i) {
+    const uint64_t hi0 = __umul64hi(M0, x[0]), lo0 = M0 * x[0];
+    const uint64_t hi1 = __umul64hi(M1, x[2]), lo1 = M1 * x[2];
+    x[0] = hi1 ^ x[1] ^ k0;
+    x[1] = lo1;
+    x[2] = hi0 ^ x[3] ^ k1;
+    x[3] = lo0;
+    k0 += 0x9E3779B97F4A7C15ull;  // golden ratio
+    k1 += 0xBB67AE8584CAA73Bull;  // sqrt(3) - 1
+  }
+}
+
+// The magnitude rounds away from zero when its fraction between the two
+// neighbours of the format, to 16 bits, is at least 1 - r / 2^16.  bf16 keeps
+// the top 16 bits of an fp32 value: adding r below them and truncating is
+// that rule (a carry moves into the exponent, or to infinity); NaN rounds to
+// nearest.
+__device__ __forceinline__ uint32_t sr_bf16(float v, uint32_t r) {
+  const uint32_t u = __float_as_uint(v);
+  if ((u & 0x7fffffffu) > 0x7f800000u) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    return *reinterpret_cast<const uint16_t*>(&b);
+  }
+  return (u + r) >> 16;
+}
+
+// fp16: v = M 2^x exactly (M the fp32 significand); the fp16 spacing at |v| is
+// 2^qe, so D = qe - x bits of M lie below it and the stored magnitude is
+// floor(M / 2^D + r / 2^16) 2^qe, formed exactly in 64-bit integers.
+__device__ __forceinline__ uint32_t sr_f16(float v, uint32_t r) {
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t mag = u & 0x7fffffffu;
+  if (mag >= 0x7f800000u) {  // infinity, NaN
+    const __half h = __float2half_rn(v);
+    return *reinterpret_cast<const uint16_t*>(&h);
+  }
+  const int E = (int)(mag >> 23);
+  const uint64_t M = E ? ((mag & 0x7fffffu) | 0x800000u) : (mag & 0x7fffffu);
+  const int x = E ? E - 150 : -149;
+  const int e = E ? E - 127 : -127;
+  const int qe = (e > -14 ? e : -14) - 10;
+  const int D = qe - x;  // 13 in the normal fp16 range, more below it
+  uint64_t t;
+  if (D >= 40) t = 0;  // M 2^-D + r 2^-16 < 1
+  else if (D >= 16) t = (M + ((uint64_t)r << (D - 16))) >> D;
+  else t = ((M << (16 - D)) + r) >> 16;
+  const float m = (float)t * __int_as_float((qe + 127) << 23);  // exact: t <= 2^11
+  const __half h = __float2half_rn(m);  // exact, or infinity past the largest value
+  return *reinterpret_cast<const uint16_t*>(&h) | ((u >> 16) & 0x8000u);
+}
+
+// Store 8 (16-bit state) or 4 (fp32) consecutive state values h (pairs) at
+// element `off` of the pool: to nearest even, or -- 16-bit state with a seed
+// -- stochastically, element e taking the 16 bits 16 (e mod 4) of word
+// (e / 4) mod 4 of Philox block e / 16 keyed by (seed, 0).
+template <class ST>
+__device__ __forceinline__ void store_state(ST* state, int64_t off, const float2* h,
+                                            const KParams& p) {
+  if constexpr (sizeof(ST) == 4) {
+    st_state(state + off, Elem<ST>::pack2(h));
+  } else {
+    if (!p.sr_seed) {
+      st_state(state + off, Elem<ST>::pack2(h));
+      return;
+    }
+    uint64_t x[4] = {(uint64_t)off >> 4, 0, 0, 0};
+    philox4x64(x, __ldg(p.sr_seed), 0, p.sr_rounds);
+    const bool upper = ((uint64_t)off >> 3) & 1;  // the chunk is half a block
+    const uint64_t w[2] = {upper ? x[2] : x[0], upper ? x[3] : x[1]};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint64_t word = w[i >> 1];
+      const uint32_t r0 = (uint32_t)(word >> (32 * (i & 1))) & 0xffffu;
+      const uint32_t r1 = (uint32_t)(word >> (32 * (i & 1) + 16)) & 0xffffu;
+      uint32_t lo, hi;
+      if constexpr (std::is_same<ST, __nv_bfloat16>::value) {
+        lo = sr_bf16(h[i].x, r0);
+        hi = sr_bf16(h[i].y, r1);
+      } else {
+        lo = sr_f16(h[i].x, r0);
+        hi = sr_f16(h[i].y, r1);
+      }
+      out[i] = (lo & 0xffffu) | (hi << 16);
+    }
+    st_state(state + off, make_uint4(out[0], out[1], out[2], out[3]));
+  }
+}
+
+// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 template <class ST, class IT, int N, int WARPS, int UNR, int LMAX>
@@ -506,8 +612,8 @@ __device__ __forceinline__ void ssu_block_on(StageT& stg, const KParams& p, int 
           if (prow < p.P) {
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c)
-              st_state(base + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
-                       Elem<ST>::pack2(&hs[u][c * L::VEC / 2]));
+              store_state<ST>(state, base - state + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
+                              &hs[u][c * L::VEC / 2], p);
           }
         }
       }

@@ -280,7 +280,6 @@ __global__ void __launch_bounds__(WARPS * 32, sizeof(ST) == 2 ? 3 : 16 / WARPS)
   constexpr int ROWS = RC::ROWS;
   constexpr int THREADS = RC::THREADS;
   constexpr int RW = UNR * L::RPW;                    // rows of one warp
-  constexpr int WBYTES = RW * N * (int)sizeof(ST);    // one warp's part of a tile
   extern __shared__ __align__(128) unsigned char smem_raw[];
   auto& m = *reinterpret_cast<typename RC::Smem*>(smem_raw);
 
@@ -455,8 +454,8 @@ __global__ void __launch_bounds__(WARPS * 32, sizeof(ST) == 2 ? 3 : 16 / WARPS)
               if (prow < p.P) {
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c)
-                  st_state(ckpt + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
-                           Elem<ST>::pack2(&hs[u][c * L::VEC / 2]));
+                  store_state<ST>(state, ckpt - state + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
+                                  &hs[u][c * L::VEC / 2], p);
               }
             }
           }
