@@ -48,10 +48,11 @@ def _workload(name, device, seed):
     from mamba2_ssm_decode_gb300 import workloads as W
     if name in W.WORKLOADS:
         return W.WORKLOADS[name](seed=seed, device=device)
-    m = re.fullmatch(r"sweep-(single|mtp)-(float32|bfloat16)-b(\d+)(-nowrite)?", name)
+    m = re.fullmatch(r"sweep-(single|mtp)-(float32|bfloat16)-b(\d+)(-nowrite)?(-sr)?", name)
     if m:
         return W.sweep_case(int(m.group(3)), getattr(torch, m.group(2)), m.group(1),
-                            disable_state_update=bool(m.group(4)), seed=seed, device=device)
+                            disable_state_update=bool(m.group(4)), seed=seed, device=device,
+                            stochastic_rounding=bool(m.group(5)))
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -204,6 +205,8 @@ class Step:
         self.launches = 1 + (2 if case.ring_start is not None and not self.replay else 0)
         self.scratch = (torch.zeros(max(1, case.nseqs), dtype=torch.int32, device=case.x.device)
                         if self.replay else None)
+        self.seed = (torch.tensor([case.sr_seed], dtype=torch.int64, device=case.x.device)
+                     if case.sr_seed is not None else None)
         if case.kind == "varlen" and case.cu_seqlens is None:
             S, T = case.nseqs, case.dense_steps
 
@@ -233,11 +236,11 @@ class Step:
                 c.ring_start, c.prev_num_accepted, c.logical_window, D=c.D, z=t["z"],
                 dt_bias=c.dt_bias, dt_softplus=c.dt_softplus, cu_seqlens=t["cu_seqlens"],
                 state_batch_indices=t["state_batch_indices"], pad_slot_id=c.pad_slot_id, out=out,
-                update_trackers=c.update_trackers, scratch=self.scratch)
+                update_trackers=c.update_trackers, scratch=self.scratch, rand_seed=self.seed)
             return
         kw = dict(D=c.D, z=t["z"], dt_bias=c.dt_bias, dt_softplus=c.dt_softplus,
                   pad_slot_id=c.pad_slot_id, disable_state_update=c.disable_state_update,
-                  out=out, algorithm=self.algorithm)
+                  out=out, algorithm=self.algorithm, rand_seed=self.seed)
         if c.kind == "single":
             self.ssu.ssu_update(c.state, t["x"], t["dt"], c.A, t["B"], t["C"],
                                 state_batch_indices=t["state_batch_indices"],
@@ -638,7 +641,8 @@ EXTRAS = ["hybrid-grouped-decode", "mtp-varlen", "replay-decode", "replay-mtp",
           "sweep-mtp-float32-b1024", "sweep-mtp-bfloat16-b1024",
           "sweep-single-bfloat16-b4096", "sweep-mtp-bfloat16-b4096",
           "sweep-single-float32-b1024-nowrite", "sweep-single-bfloat16-b1024-nowrite",
-          "sweep-mtp-float32-b1024-nowrite", "sweep-mtp-bfloat16-b1024-nowrite"]
+          "sweep-mtp-float32-b1024-nowrite", "sweep-mtp-bfloat16-b1024-nowrite",
+          "sweep-single-bfloat16-b1024-sr", "sweep-mtp-bfloat16-b1024-sr"]
 # the largest single-GPU points, measured like the headline (every timed step,
 # end to end, oracle baseline and parity sample)
 LARGE = ["sweep-single-float32-b4096", "sweep-mtp-float32-b4096"]

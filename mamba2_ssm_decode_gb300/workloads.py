@@ -62,6 +62,8 @@ class SSUCase:
     B_cache: torch.Tensor | None = None   # [slots, G, R, N]
     dt_cache: torch.Tensor | None = None  # [slots, H, R] fp32
     update_trackers: bool = False
+    # stochastic rounding of 16-bit state: the call's random seed (None: off)
+    sr_seed: int | None = None
 
     @property
     def rows(self) -> int:
@@ -354,7 +356,7 @@ def mtp_varlen_dt_per_dim(seed=0, device="cpu") -> SSUCase:
 
 
 def sweep_case(batch, state_dtype, mode, disable_state_update=False, seed=0,
-               device="cpu") -> SSUCase:
+               device="cpu", stochastic_rounding=False) -> SSUCase:
     """Large-batch sweep point: 128 heads, headdim 64, dstate 128, 8 groups,
     int64 slot tables with 2% pad sequences, z on.  mode "single": pool 2*batch;
     mode "mtp": dense 4-step call, one [batch, 4] read/write table of distinct
@@ -362,20 +364,26 @@ def sweep_case(batch, state_dtype, mode, disable_state_update=False, seed=0,
     name = f"sweep-{mode}-{str(state_dtype).split('.')[-1]}-b{batch}"
     if disable_state_update:
         name += "-nowrite"
+    if stochastic_rounding:
+        name += "-sr"
     if mode == "single":
-        return single_token_case(batch=batch, heads=128, headdim=64, dstate=128, groups=8,
-                                 slots=2 * batch, state_dtype=state_dtype, pad_frac=0.02,
-                                 index_dtype=torch.int64,
-                                 disable_state_update=disable_state_update, seed=seed,
-                                 device=device, name=name)
-    if mode == "mtp":
-        return varlen_case(nseqs=batch, max_len=4, fixed_len=4, heads=128, headdim=64,
-                           dstate=128, groups=8, slots=4 * batch, state_dtype=state_dtype,
-                           pad_frac=0.02, index_dtype=torch.int64, meta_dtype=torch.int64,
-                           same_tables=True, dense=True,
-                           disable_state_update=disable_state_update, seed=seed,
-                           device=device, name=name)
-    raise ValueError(mode)
+        c = single_token_case(batch=batch, heads=128, headdim=64, dstate=128, groups=8,
+                              slots=2 * batch, state_dtype=state_dtype, pad_frac=0.02,
+                              index_dtype=torch.int64,
+                              disable_state_update=disable_state_update, seed=seed,
+                              device=device, name=name)
+    elif mode == "mtp":
+        c = varlen_case(nseqs=batch, max_len=4, fixed_len=4, heads=128, headdim=64,
+                        dstate=128, groups=8, slots=4 * batch, state_dtype=state_dtype,
+                        pad_frac=0.02, index_dtype=torch.int64, meta_dtype=torch.int64,
+                        same_tables=True, dense=True,
+                        disable_state_update=disable_state_update, seed=seed,
+                        device=device, name=name)
+    else:
+        raise ValueError(mode)
+    if stochastic_rounding:   # a fixed seed stands in for the per-call draw
+        c.sr_seed = 0x2545F4914F6CDD1D ^ seed
+    return c
 
 
 WORKLOADS = {
