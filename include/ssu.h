@@ -394,6 +394,74 @@ ssu_status ssu_replay_update_static(const ssu_params* p, const ssu_replay_cache*
                                     int update_trackers, struct CUstream_st* stream);
 
 /*
+ * Packed variable-length SSD prefill ("mate.mamba": ssd_combined_fwd_varlen
+ * and its five stages cumsum / chunk_state / state_passing / bmm /
+ * chunk_scan).  Over the chunks of a packed batch it computes what the
+ * one-token update computes token by token -- dt' = clamp(softplus(dt +
+ * dt_bias), dt_min, dt_max) -- and returns the states at chunk ends.
+ *   x, z, out     [tokens, nheads, headdim], io_dtype (BF16 / F16),
+ *                 contiguous, 16-byte aligned; z may be NULL; out written for
+ *                 every token a chunk covers
+ *   dt            [tokens, nheads] fp32; A, dt_bias [nheads] fp32 (dt_bias
+ *                 may be NULL); D [nheads] or, with D_per_dim, [nheads,
+ *                 headdim] fp32, or NULL
+ *   B, C          [tokens, ngroups, dstate], io_dtype, contiguous
+ *   cu_chunk_seqlens [nchunks + 1]: chunk c covers tokens
+ *                 [cu[c], cu[c+1]) (at most chunk_size of them); seq_idx
+ *                 [nchunks]: the sequence owning chunk c -- a chunk opens a
+ *                 sequence when seq_idx changes, and then starts from
+ *                 initial_states[seq_idx[c]] (zeros when NULL);
+ *                 last_chunk_indices [batch]: sequence b's last chunk.  All
+ *                 meta_dtype (I32 / I64).
+ *   initial_states [batch, nheads, headdim, dstate] in initial_dtype, or NULL
+ *   states        return_intermediate_states: [nchunks, nheads, headdim,
+ *                 dstate], every chunk's end state; else [batch, ...], the
+ *                 end state of each sequence's last chunk (chunk c is
+ *                 sequence seq_idx[c]'s last when last_chunk_indices says so).
+ *                 In state_dtype (F32 / BF16 / F16), rounded to nearest even.
+ *   workspace     device memory of ssd_workspace_bytes(...) bytes, 16-byte
+ *                 aligned, owned by the caller (no contents need be kept
+ *                 between calls; calls that share it must not overlap).
+ * Supported: headdim 64, dstate 64 or 128, chunk_size a multiple of 16 up to
+ * 256.  Four kernel launches on `stream`: chunk states, state passing,
+ * C . B^T per group, the scan.
+ */
+typedef struct ssd_params {
+  const void* x;
+  const float* dt;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  int D_per_dim;
+  const void* z;
+  const float* dt_bias;
+  int dt_softplus;
+  float dt_min, dt_max;
+  void* out;
+  ssu_dtype io_dtype;
+  int64_t tokens, nheads, headdim, dstate, ngroups, chunk_size;
+  int64_t nchunks, batch;
+  const void* cu_chunk_seqlens;
+  const void* seq_idx;
+  const void* last_chunk_indices;
+  ssu_dtype meta_dtype;
+  const void* initial_states;
+  ssu_dtype initial_dtype;
+  void* states;
+  ssu_dtype state_dtype;
+  int return_intermediate_states;
+} ssd_params;
+
+/* Workspace bytes ssd_combined_fwd_varlen needs for these sizes (-1 for a
+ * negative size). */
+int64_t ssd_workspace_bytes(int64_t nchunks, int64_t nheads, int64_t ngroups, int64_t headdim,
+                            int64_t dstate, int64_t chunk_size);
+
+ssu_status ssd_combined_fwd_varlen(const ssd_params* p, void* workspace, int64_t workspace_bytes,
+                                   struct CUstream_st* stream);
+
+/*
  * Bits of the device-side error word (values, not bit positions).
  */
 #define SSU_DEVICE_ERR_COPY_TIMEOUT 1u    /* a state tile copy never landed */
@@ -431,7 +499,7 @@ const char* ssu_status_string(ssu_status status);
 const char* ssu_last_error(void);
 
 /* ABI version of this header (bumped on any incompatible change). */
-#define SSU_ABI_VERSION 3
+#define SSU_ABI_VERSION 4
 int ssu_abi_version(void);
 
 #ifdef __cplusplus

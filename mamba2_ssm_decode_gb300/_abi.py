@@ -25,7 +25,7 @@ ALGORITHMS = {"auto": SSU_ALGO_AUTO, "direct": SSU_ALGO_DIRECT, "bulk": SSU_ALGO
 # ssu_dtype
 SSU_F32, SSU_BF16, SSU_F16, SSU_I32, SSU_I64 = 0, 1, 2, 3, 4
 
-ABI_VERSION = 3
+ABI_VERSION = 4
 REPLAY_STATIC_MAX_SEQS = 65536   # SSU_REPLAY_STATIC_MAX_SEQS
 
 _c_i64 = ctypes.c_int64
@@ -75,6 +75,22 @@ class ReplayCache(ctypes.Structure):
                 ("logical_window", _c_i32)]
 
 
+class SSDParams(ctypes.Structure):
+    """struct ssd_params."""
+
+    _fields_ = [
+        ("x", _c_p), ("dt", _c_p), ("A", _c_p), ("B", _c_p), ("C", _c_p), ("D", _c_p),
+        ("D_per_dim", _c_int), ("z", _c_p), ("dt_bias", _c_p), ("dt_softplus", _c_int),
+        ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float), ("out", _c_p),
+        ("io_dtype", _c_int),
+        ("tokens", _c_i64), ("nheads", _c_i64), ("headdim", _c_i64), ("dstate", _c_i64),
+        ("ngroups", _c_i64), ("chunk_size", _c_i64), ("nchunks", _c_i64), ("batch", _c_i64),
+        ("cu_chunk_seqlens", _c_p), ("seq_idx", _c_p), ("last_chunk_indices", _c_p),
+        ("meta_dtype", _c_int), ("initial_states", _c_p), ("initial_dtype", _c_int),
+        ("states", _c_p), ("state_dtype", _c_int), ("return_intermediate_states", _c_int),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -104,6 +120,10 @@ def lib() -> ctypes.CDLL:
         L.ssu_replay_update_static.argtypes = [ctypes.POINTER(SSUParams),
                                                ctypes.POINTER(ReplayCache), _c_i64, _c_i64, _c_p,
                                                _c_int, _c_p, _c_i64, _c_int, _c_int, _c_p]
+        L.ssd_workspace_bytes.restype = _c_i64
+        L.ssd_workspace_bytes.argtypes = [_c_i64] * 6
+        L.ssd_combined_fwd_varlen.restype = _c_int
+        L.ssd_combined_fwd_varlen.argtypes = [ctypes.POINTER(SSDParams), _c_p, _c_i64, _c_p]
         L.ssu_ring_update.restype = _c_int
         L.ssu_ring_update.argtypes = [_c_p, _c_i64, _c_p, _c_i64, _c_p, _c_i64, _c_p, _c_i64,
                                       _c_int, _c_i64, _c_int, _c_i32, _c_i32, _c_i64, _c_p]

@@ -439,6 +439,117 @@ def ssu_replay_update_static(state, x, dt, A, B, C, x_cache, B_cache, dt_cache, 
     return out
 
 
+def ssd_workspace_bytes(nchunks, nheads, ngroups, headdim, dstate, chunk_size):
+    """Bytes of workspace ssd_combined_fwd_varlen needs (C ABI ``ssd_workspace_bytes``)."""
+    return int(_abi.lib().ssd_workspace_bytes(nchunks, nheads, ngroups, headdim, dstate,
+                                              chunk_size))
+
+
+def ssd_combined_fwd_varlen(x, dt, A, B, C, chunk_size, cu_seqlens, cu_chunk_seqlens,
+                            last_chunk_indices, seq_idx, out=None, D=None, z=None, dt_bias=None,
+                            dt_softplus=False, dt_limit=(0.0, float("inf")),
+                            initial_states=None, return_intermediate_states=False,
+                            state_dtype=None, workspace=None, stream=None):
+    """Packed variable-length SSD prefill (C ABI ``ssd_combined_fwd_varlen``),
+    with the call contract of "mate.mamba" ``ssd_combined_fwd_varlen``.
+
+    Returns the chunk states: [nchunks, H, P, N] with
+    ``return_intermediate_states``, else [batch, H, P, N] (the last chunk of
+    each sequence), in ``state_dtype`` (default: the initial states' dtype,
+    else C's).  ``out`` is written in place when given.  ``workspace`` (a
+    CUDA uint8 tensor of at least ssd_workspace_bytes(...) bytes) is allocated
+    when not given."""
+    dev = _require_cuda(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, last_chunk_indices,
+                        seq_idx, out, D, z, dt_bias, initial_states, workspace)
+    if x.dim() != 3 or dt.dim() != 2 or B.dim() != 3 or C.dim() != 3:
+        raise ValueError("packed SSD expects x [tokens, heads, dim] and dt [tokens, heads]")
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    if tuple(dt.shape) != (T, H):
+        raise ValueError("dt must be [tokens, heads]")
+    if x.dtype not in (torch.bfloat16, torch.float16) or B.dtype != x.dtype or C.dtype != x.dtype:
+        raise ValueError("x, B and C must share one of fp16 / bf16")
+    if dt.dtype != torch.float32:
+        raise NotImplementedError("dt must be fp32")
+    if H % G:
+        raise ValueError("heads must be divisible by groups")
+    if tuple(A.shape) != (H,) or A.dtype != torch.float32:
+        raise ValueError("A must be fp32 [heads]")
+    if dt_bias is not None and (tuple(dt_bias.shape) != (H,) or dt_bias.dtype != torch.float32):
+        raise ValueError("dt_bias must be fp32 [heads]")
+    if chunk_size <= 0:
+        raise ValueError("chunk_size must be positive")
+    nchunks = cu_chunk_seqlens.numel() - 1
+    if nchunks < 1:
+        raise ValueError("cu_chunk_seqlens must have at least two entries")
+    if seq_idx.numel() != nchunks:
+        raise ValueError("seq_idx must hold one request id per logical chunk")
+    if cu_seqlens.numel() != last_chunk_indices.numel() + 1:
+        raise ValueError("cu_seqlens and last_chunk_indices must describe the same batch")
+    batch = last_chunk_indices.numel()
+    meta = _int_dtype(cu_chunk_seqlens, "cu_chunk_seqlens")
+    for name, t in (("seq_idx", seq_idx), ("last_chunk_indices", last_chunk_indices)):
+        if _int_dtype(t, name) != meta:
+            raise ValueError("the chunk metadata must share one integer dtype")
+    if initial_states is not None:
+        if tuple(initial_states.shape) != (batch, H, P, N):
+            raise ValueError("initial_states must be [batch, heads, dim, dstate]")
+        if not initial_states.is_contiguous():
+            raise ValueError("initial_states must be contiguous")
+    if out is None:
+        out = torch.empty_like(x)
+    if out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must match x's shape and dtype")
+    D_per_dim = 0
+    if D is not None:
+        if tuple(D.shape) == (H, P):
+            D_per_dim = 1
+        elif tuple(D.shape) != (H,):
+            raise ValueError("D must be [heads, dim] or [heads]")
+        if D.dtype != torch.float32 or not D.is_contiguous():
+            raise NotImplementedError("D must be contiguous fp32")
+    if z is not None and (z.shape != x.shape or z.dtype != x.dtype or not z.is_contiguous()):
+        raise ValueError("z must match x's shape")
+    if state_dtype is None:
+        state_dtype = initial_states.dtype if initial_states is not None else C.dtype
+    if state_dtype not in _FLOAT_DT:
+        raise ValueError("state_dtype must be fp16, bf16 or fp32")
+    for t in (x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, last_chunk_indices, seq_idx):
+        if not t.is_contiguous():
+            raise ValueError("x, dt, A, B, C and the chunk metadata must be contiguous")
+    rows = nchunks if return_intermediate_states else batch
+    states = torch.empty((rows, H, P, N), dtype=state_dtype, device=dev)
+    need = ssd_workspace_bytes(nchunks, H, G, P, N, chunk_size)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    p = _abi.SSDParams()
+    p.x, p.dt, p.A, p.B, p.C = (x.data_ptr(), dt.data_ptr(), A.data_ptr(), B.data_ptr(),
+                                C.data_ptr())
+    p.D = D.data_ptr() if D is not None else None
+    p.D_per_dim = D_per_dim
+    p.z = z.data_ptr() if z is not None else None
+    p.dt_bias = dt_bias.data_ptr() if dt_bias is not None else None
+    p.dt_softplus = int(bool(dt_softplus))
+    p.dt_min, p.dt_max = float(dt_limit[0]), float(dt_limit[1])
+    p.out = out.data_ptr()
+    p.io_dtype = _FLOAT_DT[x.dtype]
+    p.tokens, p.nheads, p.headdim, p.dstate, p.ngroups = T, H, P, N, G
+    p.chunk_size, p.nchunks, p.batch = int(chunk_size), nchunks, batch
+    p.cu_chunk_seqlens = cu_chunk_seqlens.data_ptr()
+    p.seq_idx = seq_idx.data_ptr()
+    p.last_chunk_indices = last_chunk_indices.data_ptr()
+    p.meta_dtype = meta
+    p.initial_states = initial_states.data_ptr() if initial_states is not None else None
+    p.initial_dtype = _FLOAT_DT[initial_states.dtype] if initial_states is not None else 0
+    p.states = states.data_ptr()
+    p.state_dtype = _FLOAT_DT[state_dtype]
+    p.return_intermediate_states = int(bool(return_intermediate_states))
+    _abi.check(_abi.lib().ssd_combined_fwd_varlen(
+        ctypes.byref(p), ctypes.c_void_p(workspace.data_ptr()),
+        workspace.numel() * workspace.element_size(), _stream(dev, stream)))
+    return states
+
+
 def _tracker_args(ring_start, prev_num_accepted, prev_query_len, state_batch_indices):
     for name, t in (("ring_start", ring_start), ("prev_num_accepted", prev_num_accepted),
                     ("prev_query_len", prev_query_len)):

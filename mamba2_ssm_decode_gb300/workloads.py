@@ -399,6 +399,92 @@ WORKLOADS = {
 
 
 # ---------------------------------------------------------------------------
+# packed SSD prefill
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class SSDCase:
+    """One packed SSD prefill call's inputs ("mate.mamba", ssd_combined_fwd_varlen)."""
+
+    name: str
+    x: torch.Tensor                     # [tokens, H, P]
+    dt: torch.Tensor                    # [tokens, H] fp32
+    A: torch.Tensor                     # [H] fp32
+    B: torch.Tensor                     # [tokens, G, N]
+    C: torch.Tensor                     # [tokens, G, N]
+    D: torch.Tensor | None
+    z: torch.Tensor | None
+    dt_bias: torch.Tensor | None
+    chunk_size: int
+    cu_seqlens: torch.Tensor            # [batch + 1]
+    cu_chunk_seqlens: torch.Tensor      # [nchunks + 1]
+    last_chunk_indices: torch.Tensor    # [batch]
+    seq_idx: torch.Tensor               # [nchunks]
+    initial_states: torch.Tensor | None  # [batch, H, P, N]
+    dt_softplus: bool = True
+    dt_limit: tuple = (0.0, float("inf"))
+
+    def to(self, device) -> "SSDCase":
+        kw = {}
+        for f in dataclasses.fields(self):
+            v = getattr(self, f.name)
+            kw[f.name] = v.to(device) if isinstance(v, torch.Tensor) else v
+        return SSDCase(**kw)
+
+
+def chunk_metadata(lengths, chunk_size, index_dtype=torch.int64, device="cpu"):
+    """cu_seqlens, cu_chunk_seqlens, seq_idx, last_chunk_indices of a packed
+    batch: every sequence is cut into chunks of chunk_size tokens (its last one
+    shorter), as the pages' caller does."""
+    cu, cuc, seq, last = [0], [0], [], []
+    for b, L in enumerate(lengths):
+        start, pos = cu[-1], 0
+        while pos < L:
+            n = min(chunk_size, L - pos)
+            pos += n
+            cuc.append(start + pos)
+            seq.append(b)
+        last.append(len(seq) - 1)
+        cu.append(start + L)
+    return [torch.tensor(v, dtype=index_dtype, device=device) for v in (cu, cuc, seq, last)]
+
+
+def ssd_case(*, lengths, heads, headdim, dstate, groups, chunk_size=256,
+             io_dtype=torch.bfloat16, init_dtype=torch.float32, with_init=True, with_z=True,
+             D_per_dim=False, index_dtype=torch.int64, seed=0, device="cpu",
+             name="ssd") -> SSDCase:
+    """Seeded SSD prefill inputs: the decode distributions (x, z, B, C ~N(0, 1),
+    dt ~N(0, 1), dt_bias U[-4, -1], A = -exp(U[0, ln 16]), D U[0, 1]),
+    initial states ~N(0, 0.1^2)."""
+    g = _gen(seed, device)
+    T = int(sum(lengths))
+    x = _normal((T, heads, headdim), 1.0, io_dtype, g, device)
+    dt = _normal((T, heads), 1.0, torch.float32, g, device)
+    A, D, dt_bias = _head_params(heads, g, device)
+    if D_per_dim:
+        D = _uniform((heads, headdim), 0.0, 1.0, g, device)
+    B = _normal((T, groups, dstate), 1.0, io_dtype, g, device)
+    C = _normal((T, groups, dstate), 1.0, io_dtype, g, device)
+    z = _normal((T, heads, headdim), 1.0, io_dtype, g, device) if with_z else None
+    init = (_normal((len(lengths), heads, headdim, dstate), 0.1, init_dtype, g, device)
+            if with_init else None)
+    cu, cuc, seq, last = chunk_metadata(lengths, chunk_size, index_dtype, device)
+    return SSDCase(name=name, x=x, dt=dt, A=A, B=B, C=C, D=D, z=z, dt_bias=dt_bias,
+                   chunk_size=chunk_size, cu_seqlens=cu, cu_chunk_seqlens=cuc,
+                   last_chunk_indices=last, seq_idx=seq, initial_states=init)
+
+
+def ssd_prefill(seed=0, device="cpu") -> SSDCase:
+    """Packed SSD prefill shaped like the Mamba2-2.7B layer: 16 sequences of
+    U{256..2048} tokens (seeded), 80 heads, headdim 64, dstate 128, 1 group,
+    chunks of 256 tokens, bf16 x / B / C / z, fp32 initial states."""
+    g = torch.Generator().manual_seed(1000 + seed)
+    lengths = torch.randint(256, 2049, (16,), generator=g).tolist()
+    return ssd_case(lengths=lengths, heads=80, headdim=64, dstate=128, groups=1,
+                    chunk_size=256, seed=seed, device=device, name="ssd-prefill-2.7b")
+
+
+# ---------------------------------------------------------------------------
 # selecting sequences of a case (no arithmetic: rows, slots and tables only)
 # ---------------------------------------------------------------------------
 

@@ -29,7 +29,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(ssu_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(ss[ud]_\w+)\s*\(", text, flags=re.M)))
 
 
 def test_exports_every_declared_function(lib):
@@ -56,6 +56,9 @@ def test_struct_layout_matches_header(tmp_path):
     src += [f'printf("%zu\\n", offsetof(ssu_slot_table, {f}));' for f in tfields]
     src.append('printf("%zu\\n", sizeof(ssu_replay_cache));')
     src += [f'printf("%zu\\n", offsetof(ssu_replay_cache, {f}));' for f in rfields]
+    sfields = [f for f, _ in _abi.SSDParams._fields_]
+    src.append('printf("%zu\\n", sizeof(ssd_params));')
+    src += [f'printf("%zu\\n", offsetof(ssd_params, {f}));' for f in sfields]
     src.append('printf("%zu\\n", sizeof(ssu_dtype)); return 0; }')
     c = tmp_path / "layout.c"
     c.write_text("\n".join(src))
@@ -67,6 +70,7 @@ def test_struct_layout_matches_header(tmp_path):
     want += [ctypes.sizeof(_abi.SlotTable)] + [getattr(_abi.SlotTable, f).offset for f in tfields]
     want += [ctypes.sizeof(_abi.ReplayCache)]
     want += [getattr(_abi.ReplayCache, f).offset for f in rfields]
+    want += [ctypes.sizeof(_abi.SSDParams)] + [getattr(_abi.SSDParams, f).offset for f in sfields]
     want += [ctypes.sizeof(ctypes.c_int)]
     assert vals == want
 
@@ -201,6 +205,35 @@ def test_replay_rejections(lib):
     assert "scratch" in lib.ssu_last_error().decode()
     assert call_replay(lib, p, update=1, scratch=FAKE, sbytes=7) == _abi.SSU_ERR_INVALID_ARGUMENT
     assert call_replay(lib, p, nseqs=0, rows=0) == _abi.SSU_OK
+
+
+def test_ssd_rejections(lib):
+    def params(**over):
+        p = _abi.SSDParams()
+        p.x = p.dt = p.A = p.B = p.C = p.out = p.states = FAKE
+        p.cu_chunk_seqlens = p.seq_idx = p.last_chunk_indices = FAKE
+        p.io_dtype, p.meta_dtype, p.state_dtype = _abi.SSU_BF16, _abi.SSU_I64, _abi.SSU_F32
+        p.tokens, p.nheads, p.headdim, p.dstate, p.ngroups = 512, 8, 64, 128, 2
+        p.chunk_size, p.nchunks, p.batch = 256, 2, 1
+        p.dt_min, p.dt_max = 0.0, float("inf")
+        for k, v in over.items():
+            setattr(p, k, v)
+        return p
+
+    need = lib.ssd_workspace_bytes(2, 8, 2, 64, 128, 256)
+    assert need > 0 and lib.ssd_workspace_bytes(-1, 8, 2, 64, 128, 256) == -1
+    call = lambda p, ws=FAKE, n=need: lib.ssd_combined_fwd_varlen(  # noqa: E731
+        ctypes.byref(p), ws, n, None)
+    assert call(params(headdim=32)) == _abi.SSU_ERR_UNSUPPORTED
+    assert call(params(chunk_size=512)) == _abi.SSU_ERR_UNSUPPORTED
+    assert call(params(chunk_size=0)) == _abi.SSU_ERR_INVALID_ARGUMENT
+    assert call(params(ngroups=3)) == _abi.SSU_ERR_INVALID_ARGUMENT
+    assert call(params(io_dtype=_abi.SSU_F32)) == _abi.SSU_ERR_INVALID_ARGUMENT
+    assert call(params(nchunks=0)) == _abi.SSU_ERR_INVALID_ARGUMENT
+    assert call(params(dt_min=1.0, dt_max=0.5)) == _abi.SSU_ERR_INVALID_ARGUMENT
+    assert call(params(x=FAKE + 8)) == _abi.SSU_ERR_INVALID_ARGUMENT
+    assert call(params(), n=need - 1) == _abi.SSU_ERR_INVALID_ARGUMENT
+    assert "workspace" in lib.ssu_last_error().decode()
 
 
 def test_status_strings(lib):
