@@ -8,6 +8,10 @@ inputs (resident in HBM): for the default workload (Mamba2-2.7B-shaped
 decode: batch 256, 80 heads, headdim 64, dstate 128, fp32 state pool of 512
 slots, 5% pad) that is one ssu_update launch; for the MTP workload one
 ssu_update_varlen launch plus the ReplaySSM tracker update and commit.
+With extras on, the line also carries the packed SSD prefill
+(`ssd_prefill`: 16 sequences of 256..2048 tokens, Mamba2-2.7B layer shape,
+one ssd_combined_fwd_varlen call per step); `--workload ssd-prefill-2.7b`
+measures that call alone.
 
 Prints ONE JSON line.  `value` is decode tokens/s (non-pad tokens of all ranks
 / max-over-ranks time); the line also carries achieved HBM GB/s of the SSU
@@ -435,26 +439,35 @@ def measured_peak():
 DATA = "synthetic (seeded random inputs of Mamba2 serving shapes)"
 
 
-def kernel_source_hash():
+def kernel_source_hash(workload=None):
+    """Hash of the CUDA sources a workload's kernels are built from: the SSD
+    prefill's (ssd*.cu and the two headers it includes) or the SSU decode's
+    (every other source), so that a change to one leaves the other's ncu
+    traffic record valid."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mamba2_ssm_decode_gb300", "csrc")
+    ssd = workload == SSD_WORKLOAD
     for f in sorted(os.listdir(csrc)):
+        if f.startswith("ssd") != ssd and not (ssd and f in ("ssu_headrun.cuh", "ssu_kernel.cuh")):
+            continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    valid only while the kernel sources hash to the value recorded with it."""
-    path = os.path.join(ROOT, "profiles", f"ssu_{workload}_dram.txt")
+    """DRAM bytes per launch (per call for the SSD prefill) from the committed
+    ncu summary of this workload, valid only while the kernel sources hash to
+    the value recorded with it."""
+    prefix = "" if workload == SSD_WORKLOAD else "ssu_"
+    path = os.path.join(ROOT, "profiles", f"{prefix}{workload}_dram.txt")
     try:
         text = open(path).read()
     except OSError:
         return None
     m_hash = re.search(r"^kernel_source_hash:\s*(\w+)", text, re.M)
     m_val = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-    if not (m_hash and m_val) or m_hash.group(1) != kernel_source_hash():
+    if not (m_hash and m_val) or m_hash.group(1) != kernel_source_hash(workload):
         return None
     return float(m_val.group(1))
 
@@ -648,6 +661,236 @@ EXTRAS = ["hybrid-grouped-decode", "mtp-varlen", "replay-decode", "replay-mtp",
 LARGE = ["sweep-single-float32-b4096", "sweep-mtp-float32-b4096"]
 
 
+# ---------------------------------------------------------------------------
+# packed SSD prefill
+# ---------------------------------------------------------------------------
+
+SSD_WORKLOAD = "ssd-prefill-2.7b"
+SSD_TOL = 2e-2   # |gpu - oracle| <= SSD_TOL (|oracle| + rms of the oracle's row)
+
+
+def ssd_accounting(c, state_dtype=None):
+    """(tokens, algorithmic bytes, algorithmic flops) of one packed SSD call.
+
+    Bytes: x, z, B, C, dt read and y written once per token, the initial
+    states read and the final states written once per sequence, plus the
+    chunk metadata; the chunk states the call keeps in its workspace are not
+    algorithmic.  Flops (2 per multiply-add) of the contractions: the chunk
+    states (P x N per token and head), C . h_enter (the same), the
+    intra-chunk products (P per pair s <= t and head) and C . B^T (N per pair
+    and group)."""
+    T, H, P = c.x.shape
+    G, N = c.B.shape[1], c.B.shape[2]
+    io = c.x.element_size()
+    batch = c.cu_seqlens.numel() - 1
+    cuc = c.cu_chunk_seqlens.cpu().long().tolist()
+    lens = [cuc[i + 1] - cuc[i] for i in range(len(cuc) - 1)]
+    tokens = cuc[-1] - cuc[0]
+    sdt = state_dtype or (c.initial_states.dtype if c.initial_states is not None else c.C.dtype)
+    hpn = H * P * N
+    nbytes = tokens * (H * P * io * (3 if c.z is not None else 2) + H * 4 + 2 * G * N * io)
+    if c.initial_states is not None:
+        nbytes += batch * hpn * c.initial_states.element_size()
+    nbytes += batch * hpn * torch.empty((), dtype=sdt).element_size()
+    nbytes += sum(t.numel() * t.element_size() for t in (c.cu_seqlens, c.cu_chunk_seqlens,
+                                                         c.seq_idx, c.last_chunk_indices))
+    flops = 4 * tokens * hpn + sum((H * P + G * N) * L * (L + 1) for L in lens)
+    return tokens, nbytes, flops
+
+
+class SSDStep:
+    """One packed SSD prefill call through the public API, with out, states
+    and workspace preallocated (the call itself allocates nothing)."""
+
+    INPUTS = ("x", "dt", "B", "C", "z", "initial_states", "cu_seqlens", "cu_chunk_seqlens",
+              "last_chunk_indices", "seq_idx")
+
+    def __init__(self, case):
+        import mamba2_ssm_decode_gb300 as ssu
+        self.ssu, self.case = ssu, case
+        c = case
+        T, H, P = c.x.shape
+        G, N = c.B.shape[1], c.B.shape[2]
+        nch = c.cu_chunk_seqlens.numel() - 1
+        batch = c.cu_seqlens.numel() - 1
+        self.out = torch.empty_like(c.x)
+        sdt = c.initial_states.dtype if c.initial_states is not None else c.C.dtype
+        self.states = torch.empty((batch, H, P, N), dtype=sdt, device=c.x.device)
+        self.workspace = torch.empty(ssu.ssd_workspace_bytes(nch, H, G, P, N, c.chunk_size),
+                                     dtype=torch.uint8, device=c.x.device)
+        self.launches = 4
+
+    def __call__(self, **over):
+        c = self.case
+        v = {n: over.get(n, getattr(c, n)) for n in self.INPUTS}
+        return self.ssu.ssd_combined_fwd_varlen(
+            v["x"], v["dt"], c.A, v["B"], v["C"], c.chunk_size, v["cu_seqlens"],
+            v["cu_chunk_seqlens"], v["last_chunk_indices"], v["seq_idx"], out=self.out,
+            D=c.D, z=v["z"], dt_bias=c.dt_bias, dt_softplus=c.dt_softplus, dt_limit=c.dt_limit,
+            initial_states=v["initial_states"], states=self.states, workspace=self.workspace)
+
+
+def _ssd_row_excess(got, ref):
+    """max over elements of |got - ref| / (SSD_TOL (|ref| + rms of ref's row)),
+    a row being the last axis, floored at 1e-3 of the global rms."""
+    import numpy as np
+    got = got.detach().cpu().double().numpy()
+    if ref.size == 0:
+        return 0.0
+    if not np.isfinite(got).all():
+        return float("inf")
+    row = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
+    row = np.maximum(row, 1e-3 * float(np.sqrt(np.mean(ref * ref))))
+    return float((np.abs(got - ref) / (SSD_TOL * (np.abs(ref) + row))).max())
+
+
+def ssd_cpu_leg(step, nseqs=2):
+    """The fp64 SSD oracle on the first `nseqs` sequences (a bounded sample:
+    sequences are independent, so their tokens, chunks and states are a slice
+    of the batch): its rate on one host core, and the GPU call's y and final
+    states of those sequences against it."""
+    from mamba2_ssm_decode_gb300 import workloads as W
+    from oracle import ssd as ssd_oracle
+    c = step.case
+    torch.cuda.synchronize()
+    step()
+    torch.cuda.synchronize()
+    cu = c.cu_seqlens.cpu().tolist()
+    last = c.last_chunk_indices.cpu().tolist()
+    nb = min(nseqs, len(last))
+    T, nch = cu[nb], last[nb - 1] + 1
+    sub = W.SSDCase(name="sample", x=c.x[:T], dt=c.dt[:T], A=c.A, B=c.B[:T], C=c.C[:T], D=c.D,
+                    z=c.z[:T] if c.z is not None else None, dt_bias=c.dt_bias,
+                    chunk_size=c.chunk_size, cu_seqlens=c.cu_seqlens[:nb + 1],
+                    cu_chunk_seqlens=c.cu_chunk_seqlens[:nch + 1],
+                    last_chunk_indices=c.last_chunk_indices[:nb], seq_idx=c.seq_idx[:nch],
+                    initial_states=(c.initial_states[:nb] if c.initial_states is not None
+                                    else None),
+                    dt_softplus=c.dt_softplus, dt_limit=c.dt_limit).to("cpu")
+    t0 = time.perf_counter()
+    y_ref, s_ref = ssd_oracle.ssd_combined_fwd_varlen(
+        sub.x, sub.dt, sub.A, sub.B, sub.C, sub.chunk_size, sub.cu_seqlens, sub.cu_chunk_seqlens,
+        sub.last_chunk_indices, sub.seq_idx, D=sub.D, z=sub.z, dt_bias=sub.dt_bias,
+        dt_softplus=sub.dt_softplus, dt_limit=sub.dt_limit, initial_states=sub.initial_states)
+    secs = time.perf_counter() - t0
+    y_err = _ssd_row_excess(step.out[:T], y_ref)
+    s_err = _ssd_row_excess(step.states[:nb], s_ref)
+    return {"value": T / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"the first {nb} of the {len(last)} sequences of {c.name} ({T} tokens, "
+                      f"{nch} chunks): one pass of the fp64 numpy oracle on one host core",
+            "parity": {"sequences": nb, "tokens": T, "y_err_over_tol": y_err,
+                       "state_err_over_tol": s_err, "tol": SSD_TOL,
+                       "ok": bool(y_err <= 1.0 and s_err <= 1.0)}}
+
+
+def ssd_e2e(step, steps, warmup, stream):
+    """The SSD call through the public API with host buffers: every step copies
+    the call's inputs (x, z, dt, B, C, initial states, chunk metadata) from
+    pinned host memory, runs the call and copies y and the final states back,
+    then waits for them."""
+    c = step.case
+    host = {n: getattr(c, n).cpu().pin_memory() for n in step.INPUTS if getattr(c, n) is not None}
+    dev = {n: torch.empty_like(getattr(c, n)) for n in host}
+    y_host = torch.empty(c.x.shape, dtype=c.x.dtype).pin_memory()
+    s_host = torch.empty(step.states.shape, dtype=step.states.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y_host.numel() * y_host.element_size() + s_host.numel() * s_host.element_size()
+
+    def one():
+        with torch.cuda.stream(stream):
+            for n, t in host.items():
+                dev[n].copy_(t, non_blocking=True)
+            step(**dev)
+            y_host.copy_(step.out, non_blocking=True)
+            s_host.copy_(step.states, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    return (time.perf_counter() - t0) * 1e3 / steps, h2d, d2h
+
+
+def ssd_leg(args, device, stream, peak, peak_kind, steps, cpu=True):
+    """Every measurement of the packed SSD prefill: the timed calls (CUDA
+    events around each call on its stream: the four launches of one call are
+    one unit), the byte and flop rooflines of a call, the end-to-end rate and,
+    on request, the oracle sample with its parity check."""
+    from mamba2_ssm_decode_gb300 import workloads as W
+    case = W.ssd_prefill(seed=args.seed, device=device)
+    tokens, nbytes, flops = ssd_accounting(case)
+    step = SSDStep(case)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    clocks.mark("timed_start")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for k in range(steps):
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+    ends[-1].synchronize()
+    clocks.mark("timed_end")
+    time.sleep(0.15)
+    clocks.stop()
+    total = starts[0].elapsed_time(ends[-1])
+    call_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+    device_error = step.ssu.ssu_device_error()
+    tflops_peak = _tensor_peak()
+    achieved = nbytes / (call_ms * 1e-3) / 1e9
+    tflops = flops / (call_ms * 1e-3) / 1e12
+    T, H, P = case.x.shape
+    G, N = case.B.shape[1], case.B.shape[2]
+    e2e_ms, h2d, d2h = ssd_e2e(step, max(3, min(steps, 50)), 3, stream)
+    out = {
+        "metric": "packed SSD prefill tokens/s (1 GPU)",
+        "value": tokens * steps / (total * 1e-3), "unit": "tokens/s", "steps": steps,
+        "ms_per_step": total / steps, "higher_is_better": True, "dtype": "bf16 io, f32 state",
+        "config": {"workload": case.name, "batch": case.cu_seqlens.numel() - 1, "tokens": T,
+                   "nchunks": case.cu_chunk_seqlens.numel() - 1, "chunk_size": case.chunk_size,
+                   "nheads": H, "headdim": P, "dstate": N, "ngroups": G,
+                   "io_dtype": str(case.x.dtype)[6:],
+                   "state_dtype": str(step.states.dtype)[6:],
+                   "l2": f"no flush: each call reads and writes {nbytes / 1e9:.2f} GB > 129 MB L2"},
+        "roofline": {"bound": "hbm" if nbytes / (peak * 1e9) >= flops / (tflops_peak * 1e12)
+                     else "tensor",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": ncu_traffic(case.name),
+                     "algorithmic_bytes_per_call": nbytes, "algorithmic_flops_per_call": flops,
+                     "tflops": tflops, "tensor_peak_tflops": tflops_peak,
+                     "tensor_frac": tflops / tflops_peak, "call_ms": call_ms,
+                     "launches_per_call": step.launches,
+                     "peak_source": f"{peak_kind} hbm_gbs; measured bf16_tflops (burst)"},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": step.launches * steps,
+        "device_error": device_error,
+        "clocks": clocks.summary(),
+    }
+    if cpu and not args.no_cpu_baseline:
+        out["cpu_baseline"] = ssd_cpu_leg(step)
+    del step, case
+    torch.cuda.empty_cache()
+    return out
+
+
+def _tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
+
+
 def dist_setup(n_gpus):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -763,6 +1006,14 @@ def run_ours(args):
     stream = torch.cuda.Stream(device)
     peak, peak_kind = measured_peak()
 
+    if args.workload == SSD_WORKLOAD:   # the packed SSD prefill on its own
+        if world > 1:
+            raise SystemExit("the SSD prefill leg runs on one GPU")
+        line = ssd_leg(args, device, stream, peak, peak_kind, args.steps)
+        line.update({"n_gpus": 1, "warmup": max(3, args.warmup), "scaling": "weak",
+                     "vs_baseline": None, "data": DATA})
+        print(json.dumps(line), flush=True)
+        return
     h = headline(args.workload, args, world, device, stream, peak, peak_kind)
     line = {
         "metric": "SSU decode tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)",
@@ -789,6 +1040,8 @@ def run_ours(args):
         for name in LARGE:
             r = headline(name, args, world, device, stream, peak, peak_kind)
             line["large_batch"][r["config"]["workload"]] = r
+        line["ssd_prefill"] = ssd_leg(args, device, stream, peak, peak_kind,
+                                      max(5, min(args.steps, 200)))
         line["device_error_after_extras"] = step_error = \
             __import__("mamba2_ssm_decode_gb300").ssu_device_error()
         if step_error:

@@ -449,18 +449,19 @@ def ssd_combined_fwd_varlen(x, dt, A, B, C, chunk_size, cu_seqlens, cu_chunk_seq
                             last_chunk_indices, seq_idx, out=None, D=None, z=None, dt_bias=None,
                             dt_softplus=False, dt_limit=(0.0, float("inf")),
                             initial_states=None, return_intermediate_states=False,
-                            state_dtype=None, workspace=None, stream=None):
+                            state_dtype=None, states=None, workspace=None, stream=None):
     """Packed variable-length SSD prefill (C ABI ``ssd_combined_fwd_varlen``),
     with the call contract of "mate.mamba" ``ssd_combined_fwd_varlen``.
 
     Returns the chunk states: [nchunks, H, P, N] with
     ``return_intermediate_states``, else [batch, H, P, N] (the last chunk of
-    each sequence), in ``state_dtype`` (default: the initial states' dtype,
-    else C's).  ``out`` is written in place when given.  ``workspace`` (a
-    CUDA uint8 tensor of at least ssd_workspace_bytes(...) bytes) is allocated
-    when not given."""
+    each sequence), in ``state_dtype`` (default: ``states``' dtype when given,
+    else the initial states' dtype, else C's).  ``out`` and ``states`` are
+    written in place when given.  ``workspace`` (a CUDA uint8 tensor of at
+    least ssd_workspace_bytes(...) bytes) is allocated when not given; with
+    ``out``, ``states`` and ``workspace`` given the call allocates nothing."""
     dev = _require_cuda(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, last_chunk_indices,
-                        seq_idx, out, D, z, dt_bias, initial_states, workspace)
+                        seq_idx, out, D, z, dt_bias, initial_states, states, workspace)
     if x.dim() != 3 or dt.dim() != 2 or B.dim() != 3 or C.dim() != 3:
         raise ValueError("packed SSD expects x [tokens, heads, dim] and dt [tokens, heads]")
     T, H, P = x.shape
@@ -511,14 +512,20 @@ def ssd_combined_fwd_varlen(x, dt, A, B, C, chunk_size, cu_seqlens, cu_chunk_seq
     if z is not None and (z.shape != x.shape or z.dtype != x.dtype or not z.is_contiguous()):
         raise ValueError("z must match x's shape")
     if state_dtype is None:
-        state_dtype = initial_states.dtype if initial_states is not None else C.dtype
+        state_dtype = (states.dtype if states is not None else
+                       initial_states.dtype if initial_states is not None else C.dtype)
     if state_dtype not in _FLOAT_DT:
         raise ValueError("state_dtype must be fp16, bf16 or fp32")
     for t in (x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, last_chunk_indices, seq_idx):
         if not t.is_contiguous():
             raise ValueError("x, dt, A, B, C and the chunk metadata must be contiguous")
     rows = nchunks if return_intermediate_states else batch
-    states = torch.empty((rows, H, P, N), dtype=state_dtype, device=dev)
+    if states is None:
+        states = torch.empty((rows, H, P, N), dtype=state_dtype, device=dev)
+    elif (tuple(states.shape) != (rows, H, P, N) or states.dtype != state_dtype
+          or not states.is_contiguous()):
+        raise ValueError(f"states must be a contiguous {state_dtype} tensor of shape "
+                         f"{(rows, H, P, N)}")
     need = ssd_workspace_bytes(nchunks, H, G, P, N, chunk_size)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)

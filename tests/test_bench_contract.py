@@ -77,3 +77,28 @@ def test_cuda_arm_line():
     assert cb["single_core_value"] > 0
     # the GPU step checked against the oracle on the sample, inside the tolerances
     assert cb["parity"]["ok"] and cb["parity"]["sequences"] > 0
+
+
+@pytest.mark.gpu
+def test_ssd_prefill_line():
+    """The packed SSD prefill measured alone: per-call byte and flop rooflines,
+    the end-to-end rate with its copies, and the GPU call checked against the
+    fp64 oracle on a sample of sequences."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mamba2_ssm_decode_gb300 import build
+    build.build()
+    r, d = run_bench("--workload", "ssd-prefill-2.7b", "--steps", "5", "--warmup", "3")
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert d["metric"] == "packed SSD prefill tokens/s (1 GPU)" and d["steps"] == 5
+    assert d["config"]["workload"] == "ssd-prefill-2.7b" and d["config"]["chunk_size"] == 256
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    rf = d["roofline"]
+    assert rf["bound"] in ("hbm", "tensor") and rf["unit"] == "GB/s"
+    assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
+    assert rf["algorithmic_flops_per_call"] > 0 and 0 < rf["tensor_frac"] < 1.2
+    assert d["gpu_launches"] == 4 * 5 and d["device_error"] == 0
+    e = d["e2e"]
+    assert 0 < e["value"] and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["parity"]["ok"], cb["parity"]
