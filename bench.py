@@ -441,14 +441,15 @@ DATA = "synthetic (seeded random inputs of Mamba2 serving shapes)"
 
 def kernel_source_hash(workload=None):
     """Hash of the CUDA sources a workload's kernels are built from: the SSD
-    prefill's (ssd*.cu and the two headers it includes) or the SSU decode's
+    prefill's (ssd* and the three SSU headers it includes) or the SSU decode's
     (every other source), so that a change to one leaves the other's ncu
     traffic record valid."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mamba2_ssm_decode_gb300", "csrc")
     ssd = workload == SSD_WORKLOAD
     for f in sorted(os.listdir(csrc)):
-        if f.startswith("ssd") != ssd and not (ssd and f in ("ssu_headrun.cuh", "ssu_kernel.cuh")):
+        if f.startswith("ssd") != ssd and not (ssd and f in ("ssu_headrun.cuh", "ssu_kernel.cuh",
+                                                          "ssu_bulk.cuh")):
             continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
@@ -718,7 +719,7 @@ class SSDStep:
         self.states = torch.empty((batch, H, P, N), dtype=sdt, device=c.x.device)
         self.workspace = torch.empty(ssu.ssd_workspace_bytes(nch, H, G, P, N, c.chunk_size),
                                      dtype=torch.uint8, device=c.x.device)
-        self.launches = 4
+        self.launches = 3   # chunk states, state passing, scan
 
     def __call__(self, **over):
         c = self.case
@@ -815,7 +816,7 @@ def ssd_e2e(step, steps, warmup, stream):
 
 def ssd_leg(args, device, stream, peak, peak_kind, steps, cpu=True):
     """Every measurement of the packed SSD prefill: the timed calls (CUDA
-    events around each call on its stream: the four launches of one call are
+    events around each call on its stream: the three launches of one call are
     one unit), the byte and flop rooflines of a call, the end-to-end rate and,
     on request, the oracle sample with its parity check."""
     from mamba2_ssm_decode_gb300 import workloads as W

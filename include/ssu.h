@@ -423,8 +423,10 @@ ssu_status ssu_replay_update_static(const ssu_params* p, const ssu_replay_cache*
  *                 aligned, owned by the caller (no contents need be kept
  *                 between calls; calls that share it must not overlap).
  * Supported: headdim 64, dstate 64 or 128, chunk_size a multiple of 16 up to
- * 256.  Four kernel launches on `stream`: chunk states, state passing,
- * C . B^T per group, the scan.
+ * 256, nheads up to 65535, fewer than 2^30 chunks.  Three kernel launches on
+ * `stream`: chunk states, state passing, and the scan (which forms C . B^T
+ * itself, on the tensor cores).  A tensor-core wait that gives up sets
+ * SSU_DEVICE_ERR_MMA_TIMEOUT in the device error word (no valid call does).
  */
 typedef struct ssd_params {
   const void* x;
@@ -454,7 +456,8 @@ typedef struct ssd_params {
 } ssd_params;
 
 /* Workspace bytes ssd_combined_fwd_varlen needs for these sizes (-1 for a
- * negative size). */
+ * negative size): every chunk's local state (fp32) and entering state (two
+ * 16-bit parts), and dt' and the running sum of A dt' per token and head. */
 int64_t ssd_workspace_bytes(int64_t nchunks, int64_t nheads, int64_t ngroups, int64_t headdim,
                             int64_t dstate, int64_t chunk_size);
 
@@ -466,6 +469,7 @@ ssu_status ssd_combined_fwd_varlen(const ssd_params* p, void* workspace, int64_t
  */
 #define SSU_DEVICE_ERR_COPY_TIMEOUT 1u    /* a state tile copy never landed */
 #define SSU_DEVICE_ERR_RELEASE_TIMEOUT 2u /* a shared-memory stage was never released */
+#define SSU_DEVICE_ERR_MMA_TIMEOUT 4u     /* a tensor-core MMA or copy of the SSD scan never completed */
 
 /*
  * Device-side error word of the current device: nonzero after a kernel gave

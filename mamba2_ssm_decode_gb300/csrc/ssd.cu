@@ -9,33 +9,38 @@
 // with a_t the running sum of A dt' over the chunk:
 //   chunk_state  S      = sum_s exp(a_{L-1} - a_s) dt'_s x_s (outer) B_s
 //   passing      h_end  = exp(a_{L-1}) h_enter + S        (sequential over chunks)
-//   bmm          CB[t,s] = C_t . B_s                       (once per group)
+//   bmm          CB[t,s] = C_t . B_s
 //   chunk_scan   y_t    = sum_{s<=t} CB[t,s] exp(a_t - a_s) dt'_s x_s
 //                         + exp(a_t) C_t . h_enter + D x_t     (times silu(z_t))
-// The dense contractions (S, CB, the intra-chunk product and C . h_enter) run
-// on the tensor cores: warp-level m16n8k16 MMAs with fp32 accumulation, fed by
-// ldmatrix from padded (bank-conflict-free) shared tiles.  The inputs x, B, C
-// are 16-bit already; an operand the kernels compute (w_s x_s, the scaled CB,
-// h_enter) is split into a 16-bit high part and a 16-bit remainder and
-// multiplied twice, so that it enters the products to about 2^-16 instead of
-// 2^-8 (the outputs of these sums often cancel to far below their terms).
-// Four launches on the caller's stream, with the chunk states, dt' and a_t
-// and CB in a caller-provided workspace.
+// Three launches on the caller's stream: (1) dt', a_t and S per chunk and head
+// (cumsum + chunk_state, warp-level m16n8k16 MMAs); (2) the sequential state
+// passing, which also stores each chunk's entering state in the tensor-core
+// operand layout; (3) the scan on the fifth-generation tensor cores (tcgen05:
+// fp32 accumulators in tensor memory), which forms C . B^T itself (the bmm
+// stage) 64 source tokens at a time and feeds it, decayed and masked, straight
+// back into the intra-chunk product.  The inputs x, B, C are 16-bit already;
+// an operand the kernels compute (w_s x_s, the decayed C . B^T, h_enter) is
+// split into a 16-bit high part and a 16-bit remainder and multiplied twice,
+// so that it enters the products to about 2^-16 instead of 2^-8 (the outputs
+// of these sums often cancel to far below their terms).
 #include <cstdarg>
 #include <cstdio>
 
 #include "../../include/ssu.h"
+#include "ssd_tc.cuh"
+#include "ssu_bulk.cuh"
 #include "ssu_headrun.cuh"
 
 namespace ssu {
 ssu_status record_error(ssu_status code, const char* message);  // ssu_abi.cu
+unsigned* device_error_word();                                   // ssu_abi.cu
 }
 
 namespace ssd {
 using namespace ssu;
 
 constexpr int kMaxChunk = 256;  // largest supported chunk_size
-constexpr int kTile = 64;       // tokens per scan / bmm tile
+constexpr unsigned kErrMmaTimeout = SSU_DEVICE_ERR_MMA_TIMEOUT;
 
 struct SSDArgs {
   const void* x;
@@ -60,10 +65,12 @@ struct SSDArgs {
   void* states;
   int state_dtype;
   int intermediate;
-  float* ws_state;  // [nchunks, H, P, N]: chunk-local states, then entering states
-  float* ws_dt;     // [nchunks, H, CS]: dt'
-  float* ws_acum;   // [nchunks, H, CS]: a_t
-  float* ws_cb;     // [nchunks, G, CS, CS]: C_t . B_s (s <= t)
+  float* ws_state;      // [nchunks, H, P, N]: chunk-local states S
+  uint8_t* ws_henter;   // [nchunks, H]: entering state, high parts then remainders, 16-bit,
+                        // in the scan's operand layout (see ssd_chunk_scan_kernel)
+  float* ws_dt;         // [nchunks, H, CS]: dt'
+  float* ws_acum;       // [nchunks, H, CS]: a_t
+  unsigned* err;        // device error word
 };
 
 // v = hi + lo with hi, lo in the io dtype (lo: the rounding remainder of hi)
@@ -252,12 +259,37 @@ __global__ void __launch_bounds__(128) ssd_chunk_state_kernel(const SSDArgs a) {
 //    One CTA covers 512 values of one head; per block of chunks the CTA first
 //    tabulates each chunk's decay exp(a_{L-1}), whether it opens a sequence
 //    and where its end state goes, so that the loop itself only multiplies,
-//    adds and streams the chunk states (loaded several chunks ahead).
+//    adds and streams the chunk states (loaded several chunks ahead).  Each
+//    chunk's entering state goes to ws_henter as 16-bit high parts and
+//    remainders, laid out as the scan's B operand of C . h_enter^T: a K-major
+//    [P rows (p)] x [N (n)] tile whose 16-byte core-matrix rows (8 n of one p)
+//    sit at (n / 8) * 16 P + 16 p, high parts first, remainders P N 2 bytes on.
 // ---------------------------------------------------------------------------
 constexpr int kPassBlock = 256;  // chunks tabulated at a time
 constexpr int kPassAhead = 4;    // chunk states in flight per thread
 
-template <int P, int N>
+// hi + lo = (a, b) to 16-bit precision each: packed (low = a, high = b) pairs
+template <class IT>
+__device__ __forceinline__ void split_packed(float a, float b, uint32_t* hi, uint32_t* lo);
+
+template <>
+__device__ __forceinline__ void split_packed<__nv_bfloat16>(float a, float b, uint32_t* hi,
+                                                            uint32_t* lo) {
+  const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+  const __nv_bfloat162 l2 = __floats2bfloat162_rn(a - __low2float(h2), b - __high2float(h2));
+  *hi = *reinterpret_cast<const uint32_t*>(&h2);
+  *lo = *reinterpret_cast<const uint32_t*>(&l2);
+}
+
+template <>
+__device__ __forceinline__ void split_packed<__half>(float a, float b, uint32_t* hi, uint32_t* lo) {
+  const __half2 h2 = __floats2half2_rn(a, b);
+  const __half2 l2 = __floats2half2_rn(a - __low2float(h2), b - __high2float(h2));
+  *hi = *reinterpret_cast<const uint32_t*>(&h2);
+  *lo = *reinterpret_cast<const uint32_t*>(&l2);
+}
+
+template <class IT, int P, int N>
 __global__ void __launch_bounds__(128) ssd_state_passing_kernel(const SSDArgs a) {
   __shared__ float s_decay[kPassBlock];
   __shared__ int64_t s_seq[kPassBlock];
@@ -265,6 +297,10 @@ __global__ void __launch_bounds__(128) ssd_state_passing_kernel(const SSDArgs a)
   const int64_t HPN = (int64_t)a.H * P * N;
   const int64_t e = ((int64_t)blockIdx.x * 128 + threadIdx.x) * 4;  // < HPN (exact grid)
   const int h = (int)(((int64_t)blockIdx.x * 512) / (P * N));
+  // this thread's 4 values: (p, n .. n + 3) of head h; their 8-byte slot in
+  // the operand layout of ws_henter
+  const int el = (int)(e - (int64_t)h * P * N), pp = el / N, nn = el - pp * N;
+  const uint32_t hoff = (uint32_t)((nn >> 3) * (P * 16) + pp * 16 + (nn & 7) * 2);
   float4 hc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   int64_t prev = -1;
   for (int cb = 0; cb < a.nchunks; cb += kPassBlock) {
@@ -303,8 +339,14 @@ __global__ void __launch_bounds__(128) ssd_state_passing_kernel(const SSDArgs a)
         }
       }
       prev = sq;
-      // the entering state, for the scan
-      reinterpret_cast<float4*>(a.ws_state + (int64_t)(cb + i) * HPN + e)[0] = hc;
+      {  // the entering state, for the scan
+        uint8_t* blk = a.ws_henter + ((int64_t)(cb + i) * a.H + h) * (P * N * 4);
+        uint32_t h0, h1, l0, l1;
+        split_packed<IT>(hc.x, hc.y, &h0, &l0);
+        split_packed<IT>(hc.z, hc.w, &h1, &l1);
+        *reinterpret_cast<uint2*>(blk + hoff) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2*>(blk + P * N * 2 + hoff) = make_uint2(l0, l1);
+      }
       const float d = s_decay[i];
       hc = make_float4(d * hc.x + S.x, d * hc.y + S.y, d * hc.z + S.z, d * hc.w + S.w);
       const int64_t dst = s_dst[i];
@@ -320,222 +362,334 @@ __global__ void __launch_bounds__(128) ssd_state_passing_kernel(const SSDArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// 3. CB[t][s] = C_t . B_s for s <= t, once per chunk and group (64 x 64 tiles;
-//    exact products of 16-bit inputs, fp32 sums)
+// 3. the scan on the fifth-generation tensor cores: y of up to 128 query
+//    tokens (one t-block) of one chunk and head per CTA of 256 threads (two
+//    warpgroups).  Thread i of each warpgroup owns query row t = 128 tb + i,
+//    which is also tensor-memory lane i of every M = 128 accumulator:
+//      columns [0, 64)    C_t . h_enter             (K = N, h_enter split)
+//      columns [64, 128)  sum_s M[t,s] x_s          (K = 32 source tokens per slice)
+//      columns [128, 256) CB = C . B^T for 128 source tokens (one half of the chunk)
+//    The tensor core forms CB for source tokens [0, 128) up front and, for the
+//    second t-block, CB for [128, 256) once the first half has been read.
+//    Source slice j (tokens [32 j, 32 j + 32), up to the t-block's last row):
+//    each thread reads its row of CB, decays and masks it (M[t,s] = CB[t,s]
+//    exp(a_t - a_s) dt'_s for s <= t), splits it into high parts and
+//    remainders in shared memory (two buffers), and the tensor core adds
+//    M_j x_j while the threads go on to slice j + 1; x rows are copied
+//    (cp.async) one slice ahead.
+//    Shared-memory operands (no-swizzle canonical layouts, see ssd_tc.cuh):
+//      cq  C rows of the t-block, K-major: core-matrix row (r, n / 8) at
+//          (n / 8) 2048 + 16 r                       (LBO 2048, SBO 128)
+//      hm  h_enter high parts | remainders, K-major [64 p x N]: (p, n / 8) at
+//          (n / 8) 1024 + 16 p (LBO 1024, SBO 128), as stored by the passing
+//          kernel; once C . h_enter is done, the same bytes hold two buffers
+//          of M_j high parts | remainders, K-major [128 t x 32 s]: (t, s / 8)
+//          at (t / 8) 512 + (s / 8) 128 + 16 (t % 8)  (LBO 128, SBO 512)
+//      bs  B rows of one half (128 source tokens), K-major: (s, n / 8) at
+//          (n / 8) 2048 + 16 s                       (LBO 2048, SBO 128)
+//      xs  x rows of a slice (two buffers), MN-major [64 p x 32 s]: the 8 p
+//          of (p / 8, s) at (p / 8) 512 + 16 s       (LBO 128, SBO 512)
 // ---------------------------------------------------------------------------
-template <class IT, int N>
-__global__ void __launch_bounds__(128) ssd_bmm_kernel(const SSDArgs a) {
-  const int c = blockIdx.x, g = blockIdx.y;
-  const int tb = blockIdx.z / (kMaxChunk / kTile), sb = blockIdx.z % (kMaxChunk / kTile);
-  if (sb > tb) return;  // above the diagonal: never read
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ __align__(16) IT Cs[kTile][N + 8];
-  __shared__ __align__(16) IT Bs[kTile][N + 8];
-  int64_t t0;
-  int Lc;
-  chunk_span(a, c, &t0, &Lc);
-  if (tb * kTile >= Lc) return;
-  const IT* bg = static_cast<const IT*>(a.B);
-  const IT* cg = static_cast<const IT*>(a.C);
-  for (int i = tid; i < kTile * (N / 8); i += 128) {
-    const int r = i / (N / 8), q8 = (i - r * (N / 8)) * 8;
-    const int t = tb * kTile + r, sI = sb * kTile + r;
-    if (t < Lc) copy8(&Cs[r][q8], cg + ((t0 + t) * a.G + g) * N + q8);
-    else *reinterpret_cast<uint4*>(&Cs[r][q8]) = make_uint4(0u, 0u, 0u, 0u);
-    if (sI < Lc) copy8(&Bs[r][q8], bg + ((t0 + sI) * a.G + g) * N + q8);
-    else *reinterpret_cast<uint4*>(&Bs[r][q8]) = make_uint4(0u, 0u, 0u, 0u);
-  }
-  __syncthreads();
-  float acc[kTile / 8][4];
-#pragma unroll
-  for (int j = 0; j < kTile / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
-  const int m = lane >> 3, j8 = lane & 7;
-#pragma unroll
-  for (int ks = 0; ks < N / 16; ++ks) {
-    uint32_t af[4];  // A = C: rows t, columns n
-    ldsm_x4(af, saddr(&Cs[warp * 16 + j8 + (m & 1 ? 8 : 0)][ks * 16 + (m >= 2 ? 8 : 0)]));
-#pragma unroll
-    for (int np = 0; np < kTile / 16; ++np) {
-      uint32_t bf[4];  // B = B^T: rows n, columns s (stored [s][n])
-      ldsm_x4(bf, saddr(&Bs[np * 16 + j8 + (m >= 2 ? 8 : 0)][ks * 16 + (m & 1 ? 8 : 0)]));
-      mma_16816<IT>(acc[2 * np], af, bf[0], bf[1]);
-      mma_16816<IT>(acc[2 * np + 1], af, bf[2], bf[3]);
-    }
-  }
-  float* cb = a.ws_cb + ((int64_t)c * a.G + g) * a.CS * a.CS;
-  const int r0 = tb * kTile + warp * 16 + (lane >> 2), c0 = sb * kTile + 2 * (lane & 3);
-#pragma unroll
-  for (int j = 0; j < kTile / 8; ++j) {
-    if (c0 + j * 8 >= a.CS) break;  // chunk sizes below 64: columns past the chunk
-    if (r0 < a.CS)
-      *reinterpret_cast<float2*>(&cb[(int64_t)r0 * a.CS + c0 + j * 8]) =
-          make_float2(acc[j][0], acc[j][1]);
-    if (r0 + 8 < a.CS)
-      *reinterpret_cast<float2*>(&cb[(int64_t)(r0 + 8) * a.CS + c0 + j * 8]) =
-          make_float2(acc[j][2], acc[j][3]);
+constexpr int kTB = 128;               // query rows per CTA (the MMA M)
+constexpr int kSL = 32;                // source tokens per slice
+constexpr int kHalf = 128;             // source tokens per C . B^T block
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColInter = 0, kColIntra = 64, kColCB = 128;
+constexpr int kScanMinSmem = 78 * 1024;  // at most two CTAs per SM: 2 x 256 columns
+constexpr int kMBytes = kTB * kSL * 2;   // one part (high or remainder) of M_j
+
+template <int P, int N>
+struct ScanSmem {
+  uint8_t cq[kTB * N * 2];
+  uint8_t hm[(2 * P * N * 2 > 4 * kMBytes) ? 2 * P * N * 2 : 4 * kMBytes];
+  uint8_t bs[kHalf * N * 2];
+  uint8_t xs[2][kSL * P * 2];
+  float acum[kMaxChunk], dtp[kMaxChunk], q[kMaxChunk], qs[kMaxChunk];
+  int tame[kMaxChunk / kSL];
+  uint64_t bar_h, bar_cb, bar_intra;
+  uint32_t tmem;
+};
+
+// Spin on an mbarrier phase (the tensor core finishes within microseconds: a
+// suspended wait would add its wake-up latency); false after `limit_ns`.
+__device__ __forceinline__ bool spin_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
   }
 }
 
-// ---------------------------------------------------------------------------
-// 4. the scan: y of one chunk and head per CTA, 64 query tokens at a time
-// ---------------------------------------------------------------------------
 template <class IT, int P, int N>
-struct ScanSmem {
-  float acum[kMaxChunk], dtp[kMaxChunk];
-  IT H[2][P][N + 8];  // h_enter: high parts, remainders
-  IT Cq[kTile][N + 8];
-  IT Xs[kTile][P + 8];
-};
-
-template <class IT, int P, int N>
-__global__ void __launch_bounds__(128) ssd_chunk_scan_kernel(const SSDArgs a) {
-  const int c = blockIdx.x, h = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
+  static_assert(P == 64 && (N == 64 || N == 128), "headdim 64, dstate 64 or 128");
+  constexpr bool kBF16 = std::is_same<IT, __nv_bfloat16>::value;
+  constexpr uint32_t kIdInter = tc::idesc_f16(kBF16, kTB, 64, false, false);
+  constexpr uint32_t kIdCB = tc::idesc_f16(kBF16, kTB, kHalf, false, false);
+  constexpr uint32_t kIdIntra = tc::idesc_f16(kBF16, kTB, 64, false, true);
+  constexpr int NT = 256;
+  const int c = blockIdx.x >> 1, tb = blockIdx.x & 1, h = blockIdx.y;
+  // two warpgroups: both cover the 128 rows (tensor-memory lanes); warpgroup
+  // wg takes columns [16 wg, 16 wg + 16) of each source slice and output
+  // columns [32 wg, 32 wg + 32)
+  const int tid = threadIdx.x, warp = tid >> 5, wg = warp >> 2, lrow = tid & 127;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  auto& sm = *reinterpret_cast<ScanSmem<IT, P, N>*>(smem_raw);
+  auto& sm = *reinterpret_cast<ScanSmem<P, N>*>(smem_raw);
   int64_t t0;
   int Lc;
   chunk_span(a, c, &t0, &Lc);
-  if (Lc <= 0) return;
+  const int r0 = tb * kTB;  // this CTA's query rows [r0, tmax) of the chunk
+  if (r0 >= Lc) return;
+  if (*reinterpret_cast<volatile unsigned*>(a.err) & kErrMmaTimeout) return;  // a wait gave up
+  const int tmax = min(Lc, r0 + kTB);
+  const int J = (tmax - 1) / kSL + 1;  // source slices
   const int g = h / a.hr;
   const float* wdt = a.ws_dt + ((int64_t)c * a.H + h) * a.CS;
   const float* wac = a.ws_acum + ((int64_t)c * a.H + h) * a.CS;
-  for (int i = tid; i < Lc; i += 128) {
-    sm.dtp[i] = wdt[i];
-    sm.acum[i] = wac[i];
+  for (int i = tid; i < J * kSL; i += NT) {
+    const bool in = i < Lc;
+    sm.dtp[i] = in ? wdt[i] : 0.0f;
+    sm.acum[i] = in ? wac[i] : 0.0f;
   }
-  const float* hin = a.ws_state + ((int64_t)c * a.H + h) * P * N;
-  for (int i = tid; i < P * N / 4; i += 128) {
-    const int p = (i * 4) / N, n = (i * 4) - p * N;
-    const float4 v = *reinterpret_cast<const float4*>(&hin[p * N + n]);
-    const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) split2<IT>(vv[k], &sm.H[0][p][n + k], &sm.H[1][p][n + k]);
-  }
+  const uint32_t s_cq = smem_addr(sm.cq), s_hm = smem_addr(sm.hm), s_bs = smem_addr(sm.bs);
+  const uint32_t s_xs[2] = {smem_addr(sm.xs[0]), smem_addr(sm.xs[1])};
   const IT* cg = static_cast<const IT*>(a.C);
+  const IT* bg = static_cast<const IT*>(a.B);
   const IT* xg = static_cast<const IT*>(a.x);
-  const float* cbg = a.ws_cb + ((int64_t)c * a.G + g) * a.CS * a.CS;
+  // rows [base, base + 128) of a [tokens, groups, N] tensor (C or B), K-major
+  auto load_rows = [&](uint32_t dst, const IT* src, int base) {
+#pragma unroll 1
+    for (int q = tid; q < 128 * (N / 8); q += NT) {
+      const int r = q % 128, kg = q / 128, tk = base + r;
+      const bool ok = tk < Lc;
+      tc::cp16(dst + kg * 2048 + r * 16, src + ((t0 + (ok ? tk : 0)) * a.G + g) * N + kg * 8,
+               ok ? 16u : 0u);
+    }
+  };
+  auto load_x = [&](int j) {  // one 16-byte piece per thread
+    const int sl = tid % kSL, pg = tid / kSL, s = j * kSL + sl;
+    const bool ok = s < Lc;
+    tc::cp16(s_xs[j & 1] + pg * 512 + sl * 16, xg + ((t0 + (ok ? s : 0)) * a.H + h) * P + pg * 8,
+             ok ? 16u : 0u);
+  };
+  static_assert(kSL * (P / 8) == NT, "one x piece per thread");
+  load_rows(s_cq, cg, r0);
+  load_rows(s_bs, bg, 0);
+  load_x(0);
+  tc::cp_commit();
+  if (tid == 0) {
+    mbar_init(&sm.bar_h, 1);
+    mbar_init(&sm.bar_cb, 1);
+    mbar_init(&sm.bar_intra, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the entering state, already in operand layout: one bulk copy
+    mbar_arrive_expect_tx(&sm.bar_h, 2 * P * N * 2);
+    bulk_load(sm.hm, a.ws_henter + ((int64_t)c * a.H + h) * (P * N * 4), 2 * P * N * 2,
+              &sm.bar_h);
+  }
+  if (warp == 0) tc::alloc(smem_addr(&sm.tmem), kTmemCols);
+  __syncthreads();  // acum / dtp written
+  // per source token: exp(a_e - a_s) dt'_s and exp(a_b - a_s) dt'_s, a_b and
+  // a_e at the first and last token of its slice; per slice: whether a_b -
+  // a_e <= 60, so that the second form cannot overflow
+  for (int i = tid; i < J * kSL; i += NT) {
+    const int b = (i / kSL) * kSL, e = min(b + kSL - 1, Lc - 1);
+    sm.q[i] = i < Lc ? expf(sm.acum[e] - sm.acum[i]) * sm.dtp[i] : 0.0f;
+    sm.qs[i] = i < Lc ? expf(fminf(sm.acum[b] - sm.acum[i], 60.0f)) * sm.dtp[i] : 0.0f;
+  }
+  if (tid < J) {
+    const int b = tid * kSL, e = min(b + kSL - 1, Lc - 1);
+    sm.tame[tid] = b < Lc && sm.acum[b] - sm.acum[e] <= 60.0f;
+  }
+  tc::cp_wait<0>();  // C, B rows [0, 128), x_0
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sm.tmem;
+  bool dead = false;  // a bounded wait gave up: finish without waiting again
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    if (!dead && !spin_wait(bar, parity, kWaitLimitNs)) {
+      dead = true;
+      atomicOr(a.err, kErrMmaTimeout);
+    }
+  };
+  auto issue_cb = [&]() {  // CB of the 128 source tokens in bs
+#pragma unroll
+    for (int kk = 0; kk < N / 16; ++kk)
+      tc::mma(tmem + kColCB, tc::sdesc(s_cq + kk * 4096, 2048, 128),
+              tc::sdesc(s_bs + kk * 4096, 2048, 128), kIdCB, kk != 0);
+    tc::commit(smem_addr(&sm.bar_cb));
+  };
+  if (tid == 0) {
+    wait(&sm.bar_h, 0);
+    // C . h_enter^T, high parts then remainders
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int kk = 0; kk < N / 16; ++kk)
+        tc::mma(tmem + kColInter, tc::sdesc(s_cq + kk * 4096, 2048, 128),
+                tc::sdesc(s_hm + part * (P * N * 2) + kk * 2048, 1024, 128), kIdInter,
+                (part | kk) != 0);
+    issue_cb();
+  }
+  // a_t is non-increasing along the chunk when A <= 0 and dt' >= 0: then for
+  // a slice wholly at or before t, exp(a_t - a_s) = exp(a_t - a_e) exp(a_e - a_s)
+  // with both factors <= 1 (no overflow), one exponential per slice and row
+  const bool monotone = a.A[h] <= 0.0f && a.dt_lo >= 0.0f;
+  const int t = r0 + lrow;
+  const bool trow = t < Lc;
+  const int tt = trow ? t : -1;  // no source token is at or before a row past the chunk
+  const float at = trow ? sm.acum[t] : 0.0f;
+  const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  const int m_row = (lrow >> 3) * 512 + (lrow & 7) * 16 + wg * 256;  // + kg 128, kg in {2 wg, 2 wg + 1}
   const IT* zg = static_cast<const IT*>(a.z);
-  IT* og = static_cast<IT*>(a.out);
-  const int m = lane >> 3, j8 = lane & 7;
-  const int rl = warp * 16 + (lane >> 2);  // this thread's rows rl, rl + 8 of a query tile
-  const int c0 = 2 * (lane & 3);
-  constexpr int PT = P / 8;
-
-  for (int q0 = 0; q0 < Lc; q0 += kTile) {
-    __syncthreads();  // the previous query tile's buffers are free
-    for (int i = tid; i < kTile * (N / 8); i += 128) {
-      const int r = i / (N / 8), q8 = (i - r * (N / 8)) * 8;
-      const int t = q0 + r;
-      if (t < Lc) copy8(&sm.Cq[r][q8], cg + ((t0 + t) * a.G + g) * N + q8);
-      else *reinterpret_cast<uint4*>(&sm.Cq[r][q8]) = make_uint4(0u, 0u, 0u, 0u);
+  const int64_t row = trow ? ((t0 + t) * a.H + h) * P : 0;
+  uint32_t ph_cb = 0, ph_in = 0;
+  for (int j = 0; j < J; ++j) {
+    const int s0 = j * kSL;
+    if ((s0 % kHalf) == 0) {  // a new C . B^T block: wait for it
+      wait(&sm.bar_cb, ph_cb);
+      ph_cb ^= 1;
+      tc::fence_after_sync();
     }
-    __syncthreads();
-    // C_t . h_enter (A = C rows t; B = h^T, stored [p][n]), high parts + remainders
-    float yi[PT][4];
-#pragma unroll
-    for (int jj = 0; jj < PT; ++jj) yi[jj][0] = yi[jj][1] = yi[jj][2] = yi[jj][3] = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < N / 16; ++ks) {
-      uint32_t af[4];
-      ldsm_x4(af, saddr(&sm.Cq[warp * 16 + j8 + (m & 1 ? 8 : 0)][ks * 16 + (m >= 2 ? 8 : 0)]));
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-#pragma unroll
-        for (int np = 0; np < PT / 2; ++np) {
-          uint32_t bf[4];
-          ldsm_x4(bf, saddr(&sm.H[part][np * 16 + j8 + (m >= 2 ? 8 : 0)]
-                                     [ks * 16 + (m & 1 ? 8 : 0)]));
-          mma_16816<IT>(yi[2 * np], af, bf[0], bf[1]);
-          mma_16816<IT>(yi[2 * np + 1], af, bf[2], bf[3]);
-        }
-      }
+    if (j == J - 1 && trow && wg == 0) {  // this row's x and z (one 128-byte line each) into L1
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(xg + row));
+      if (zg) asm volatile("prefetch.global.L1 [%0];" ::"l"(zg + row));
     }
-    const int tA = q0 + rl, tB = tA + 8;
-    const float aA = tA < Lc ? sm.acum[tA] : 0.0f, aB = tB < Lc ? sm.acum[tB] : 0.0f;
-    // sum_{s <= t} (C_t . B_s) exp(a_t - a_s) dt'_s x_s, 64 source tokens at a time
-    float yo[PT][4];
-#pragma unroll
-    for (int jj = 0; jj < PT; ++jj) yo[jj][0] = yo[jj][1] = yo[jj][2] = yo[jj][3] = 0.0f;
-    for (int s0 = 0; s0 <= q0; s0 += kTile) {
-      // this thread's CB values (rows tA, tB; the accumulator layout), issued
-      // before the x tile is staged
-      float cb[kTile / 8][4];
-#pragma unroll
-      for (int jj = 0; jj < kTile / 8; ++jj) {
-        const int sI = s0 + jj * 8 + c0;  // even: sI + 1 < CS whenever sI < Lc
-        float2 u = make_float2(0.0f, 0.0f), w = make_float2(0.0f, 0.0f);
-        if (sI < Lc && tA < Lc) u = *reinterpret_cast<const float2*>(&cbg[(int64_t)tA * a.CS + sI]);
-        if (sI < Lc && tB < Lc) w = *reinterpret_cast<const float2*>(&cbg[(int64_t)tB * a.CS + sI]);
-        cb[jj][0] = u.x;
-        cb[jj][1] = u.y;
-        cb[jj][2] = w.x;
-        cb[jj][3] = w.y;
-      }
-      __syncthreads();  // the previous source tile is free
-      for (int i = tid; i < kTile * (P / 8); i += 128) {
-        const int r = i / (P / 8), q8 = (i - r * (P / 8)) * 8;
-        const int sI = s0 + r;
-        if (sI < Lc) copy8(&sm.Xs[r][q8], xg + ((t0 + sI) * a.H + h) * P + q8);
-        else *reinterpret_cast<uint4*>(&sm.Xs[r][q8]) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      __syncthreads();
-      // scale by exp(a_t - a_s) dt'_s, mask s > t, split into A fragments
-      uint32_t ph[kTile / 16][4], pl[kTile / 16][4];
-#pragma unroll
-      for (int jj = 0; jj < kTile / 8; ++jj) {
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int sI = s0 + jj * 8 + c0 + e;
-          const bool in = sI < Lc;
-          const float ws = in ? sm.dtp[sI] : 0.0f, as = in ? sm.acum[sI] : 0.0f;
-          v[e] = (in && sI <= tA && tA < Lc) ? cb[jj][e] * expf(aA - as) * ws : 0.0f;
-          v[2 + e] = (in && sI <= tB && tB < Lc) ? cb[jj][2 + e] * expf(aB - as) * ws : 0.0f;
-        }
-        const int kb = jj >> 1, half = jj & 1;
-        split_pair<IT>(v[0], v[1], &ph[kb][half * 2], &pl[kb][half * 2]);
-        split_pair<IT>(v[2], v[3], &ph[kb][half * 2 + 1], &pl[kb][half * 2 + 1]);
-      }
-#pragma unroll
-      for (int kb = 0; kb < kTile / 16; ++kb) {
-#pragma unroll
-        for (int np = 0; np < PT / 2; ++np) {
-          uint32_t bf[4];  // B = x: rows s, columns p (stored [s][p]: transposed loads)
-          ldsm_x4_t(bf, saddr(&sm.Xs[kb * 16 + j8 + (m & 1 ? 8 : 0)][np * 16 + (m >= 2 ? 8 : 0)]));
-          mma_16816<IT>(yo[2 * np], ph[kb], bf[0], bf[1]);
-          mma_16816<IT>(yo[2 * np + 1], ph[kb], bf[2], bf[3]);
-          mma_16816<IT>(yo[2 * np], pl[kb], bf[0], bf[1]);
-          mma_16816<IT>(yo[2 * np + 1], pl[kb], bf[2], bf[3]);
-        }
+    // M_j, row t, columns [16 wg, 16 wg + 16) of the slice, into buffer j % 2
+    // (free: M_{j-2} x_{j-2} is done)
+    float cb[16];
+    tc::ld16(lane_base + kColCB + (s0 % kHalf) + 16 * wg, cb);
+    tc::wait_ld();
+    const int sb = s0 + 16 * wg;  // first source token of this thread's columns
+    // With a_t non-increasing, exp(a_t - a_s) = exp(a_t - a_ref) exp(a_ref - a_s):
+    // a slice wholly at or before t takes a_ref = its last token (both factors
+    // <= 1); the slice holding t takes a_ref = its first token when the slice
+    // decays by at most e^60 (first factor <= 1, second <= e^60); otherwise one
+    // exponential per entry.
+    const float* tab = sm.q;
+    float rf = 0.0f;
+    bool per_entry = false;
+    if (s0 <= tt) {
+      if (monotone && s0 + kSL - 1 <= tt) {
+        rf = expf(at - sm.acum[s0 + kSL - 1]);
+      } else if (monotone && sm.tame[j]) {
+        rf = expf(at - sm.acum[s0]);
+        tab = sm.qs;
+      } else {
+        per_entry = true;
       }
     }
-    // y = intra + exp(a_t) C_t . h_enter + D x_t, times silu(z_t)
+    uint8_t* m_hi = sm.hm + (j & 1) * (2 * kMBytes) + m_row;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int t = half ? tB : tA;
-      if (t >= Lc) continue;
-      const float dec = expf(half ? aB : aA);
-      const int64_t row = ((t0 + t) * a.H + h) * P;
+    for (int kh = 0; kh < 2; ++kh) {
+      uint32_t hp[4], lp[4];
 #pragma unroll
-      for (int jj = 0; jj < PT; ++jj) {
-        const int p = jj * 8 + c0;
+      for (int k = 0; k < 8; k += 2) {
         float v[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          float y = yo[jj][half * 2 + e] + dec * yi[jj][half * 2 + e];
-          const float xv = io_to_float<IT>(xg[row + p + e]);
-          if (a.D) y += (a.D_per_dim ? a.D[h * P + p + e] : a.D[h]) * xv;
+          const int s = sb + kh * 8 + k + e;
+          float f;
+          if (!per_entry) f = s <= tt ? rf * tab[s] : 0.0f;
+          else f = s <= tt ? __expf(at - sm.acum[s]) * sm.dtp[s] : 0.0f;
+          v[e] = cb[kh * 8 + k + e] * f;
+        }
+        split_packed<IT>(v[0], v[1], &hp[k / 2], &lp[k / 2]);
+      }
+      *reinterpret_cast<uint4*>(m_hi + kh * 128) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+      *reinterpret_cast<uint4*>(m_hi + kMBytes + kh * 128) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
+    }
+    if (s0 + kSL == kHalf && J * kSL > kHalf) {
+      // every row of the first half's CB is read: B rows [128, 256) into bs
+      // (CB of the first half is done with it), then C . B^T of the second half
+      tc::fence_before_sync();
+      __syncthreads();
+      load_rows(s_bs, bg, kHalf);
+      tc::cp_commit();
+      tc::cp_wait<0>();
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+      if (tid == 0) issue_cb();
+    }
+    if (j > 0) {  // M_{j-1} x_{j-1} done: x buffer (j + 1) % 2 and M buffer (j + 1) % 2 free
+      wait(&sm.bar_intra, ph_in);
+      ph_in ^= 1;
+    }
+    if (j + 1 < J) load_x(j + 1);
+    tc::cp_commit();
+    tc::cp_wait<1>();  // all but x_{j+1}: x_j has landed
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid == 0) {
+      // sum_s M[t,s] x_s: high parts, then remainders
+      const uint32_t s_m = s_hm + (j & 1) * (2 * kMBytes);
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int kk = 0; kk < kSL / 16; ++kk)
+          tc::mma(tmem + kColIntra, tc::sdesc(s_m + part * kMBytes + kk * 256, 128, 512),
+                  tc::sdesc(s_xs[j & 1] + kk * 256, 128, 512), kIdIntra, (j | part | kk) != 0);
+      tc::commit(smem_addr(&sm.bar_intra));
+    }
+  }
+  wait(&sm.bar_intra, ph_in);  // the last M x done: every accumulator is final
+  tc::fence_after_sync();
+  // y = intra + exp(a_t) C_t . h_enter + D x_t, times silu(z_t): output
+  // columns [32 wg, 32 wg + 32) of row t
+  IT* og = static_cast<IT*>(a.out);
+  const float dec = expf(at);
+  const float Dh = (a.D && !a.D_per_dim) ? a.D[h] : 0.0f;
+#pragma unroll 1
+  for (int c16 = 2 * wg; c16 < 2 * wg + 2; ++c16) {
+    float yi[16], yo[16];
+    tc::ld16(lane_base + kColInter + c16 * 16, yi);
+    tc::ld16(lane_base + kColIntra + c16 * 16, yo);
+    uint4 xq[2], zq[2];
+    if (trow) {
+      xq[0] = __ldg(reinterpret_cast<const uint4*>(xg + row) + 2 * c16);
+      xq[1] = __ldg(reinterpret_cast<const uint4*>(xg + row) + 2 * c16 + 1);
+      zq[0] = zg ? __ldg(reinterpret_cast<const uint4*>(zg + row) + 2 * c16) : make_uint4(0u, 0u, 0u, 0u);
+      zq[1] = zg ? __ldg(reinterpret_cast<const uint4*>(zg + row) + 2 * c16 + 1)
+                 : make_uint4(0u, 0u, 0u, 0u);
+    }
+    tc::wait_ld();
+    if (trow) {
+      const IT* xv = reinterpret_cast<const IT*>(&xq[0]);
+      const IT* zv = reinterpret_cast<const IT*>(&zq[0]);
+      uint32_t packed[8];
+#pragma unroll
+      for (int k = 0; k < 16; k += 2) {
+        float v[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int p = c16 * 16 + k + e;
+          float y = yo[k + e] + dec * yi[k + e];
+          const float x = io_to_float<IT>(xv[k + e]);
+          if (a.D) y += (a.D_per_dim ? a.D[h * P + p] : Dh) * x;
           if (zg) {
-            const float zv = io_to_float<IT>(zg[row + p + e]);
-            y *= zv / (1.0f + expf(-zv));
+            const float zz = io_to_float<IT>(zv[k + e]);
+            y *= zz * __frcp_rn(1.0f + __expf(-zz));
           }
           v[e] = y;
         }
-        *reinterpret_cast<uint32_t*>(&og[row + p]) = pack_pair<IT>(v[0], v[1]);
+        packed[k / 2] = pack_pair<IT>(v[0], v[1]);
       }
+      reinterpret_cast<uint4*>(og + row)[2 * c16] =
+          make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      reinterpret_cast<uint4*>(og + row)[2 * c16 + 1] =
+          make_uint4(packed[4], packed[5], packed[6], packed[7]);
     }
   }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tmem, kTmemCols);
 }
 
 template <class IT, int P, int N>
@@ -544,24 +698,25 @@ cudaError_t launch(const SSDArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   static_assert((P * N) % 512 == 0, "a state-passing CTA covers 512 values of one head");
-  ssd_state_passing_kernel<P, N><<<(unsigned)((int64_t)a.H * P * N / 512), 128, 0, stream>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  constexpr int TB = kMaxChunk / kTile;
-  ssd_bmm_kernel<IT, N><<<dim3(a.nchunks, a.G, TB * TB), 128, 0, stream>>>(a);
+  ssd_state_passing_kernel<IT, P, N>
+      <<<(unsigned)((int64_t)a.H * P * N / 512), 128, 0, stream>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto scan = ssd_chunk_scan_kernel<IT, P, N>;
-  const int smem = (int)sizeof(ScanSmem<IT, P, N>);
+  const int smem = (int)sizeof(ScanSmem<P, N>) > kScanMinSmem ? (int)sizeof(ScanSmem<P, N>)
+                                                                : kScanMinSmem;
   if ((e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
       cudaSuccess)
     return e;
-  scan<<<dim3(a.nchunks, a.H), 128, smem, stream>>>(a);
+  scan<<<dim3((unsigned)a.nchunks * 2, a.H), 256, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
+// chunk states (fp32), entering states (16-bit pairs), dt', a_t
 int64_t workspace_bytes(int64_t nchunks, int64_t H, int64_t G, int64_t P, int64_t N,
                         int64_t CS) {
+  (void)G;
   auto up = [](int64_t b) { return (b + 255) / 256 * 256; };
-  return up(nchunks * H * P * N * 4) + 2 * up(nchunks * H * CS * 4) + up(nchunks * G * CS * CS * 4);
+  return 2 * up(nchunks * H * P * N * 4) + 2 * up(nchunks * H * CS * 4);
 }
 
 }  // namespace ssd
@@ -607,8 +762,8 @@ ssu_status ssd_combined_fwd_varlen(const ssd_params* p, void* workspace, int64_t
                (long long)p->chunk_size);
   if (p->nchunks < 1) return bad(SSU_ERR_INVALID_ARGUMENT, "cu_chunk_seqlens must have at least two entries");
   if (p->batch < 0) return bad(SSU_ERR_INVALID_ARGUMENT, "batch must be >= 0");
-  if (p->tokens > 0x7fffffffLL || p->nchunks > 0x7fffffffLL)
-    return bad(SSU_ERR_UNSUPPORTED, "tokens and chunks must be below 2^31");
+  if (p->tokens > 0x7fffffffLL || p->nchunks > 0x3fffffffLL || p->nheads > 65535)
+    return bad(SSU_ERR_UNSUPPORTED, "tokens below 2^31, chunks below 2^30 and heads up to 65535");
   if (!is_idx(p->meta_dtype))
     return bad(SSU_ERR_INVALID_ARGUMENT, "chunk metadata must be int32 or int64");
   if (!is_float(p->state_dtype)) return bad(SSU_ERR_INVALID_ARGUMENT, "state_dtype must be fp32, bf16 or fp16");
@@ -659,11 +814,13 @@ ssu_status ssd_combined_fwd_varlen(const ssd_params* p, void* workspace, int64_t
   auto up = [](int64_t b) { return (b + 255) / 256 * 256; };
   a.ws_state = reinterpret_cast<float*>(ws);
   ws += up(p->nchunks * p->nheads * p->headdim * p->dstate * 4);
+  a.ws_henter = reinterpret_cast<uint8_t*>(ws);
+  ws += up(p->nchunks * p->nheads * p->headdim * p->dstate * 4);
   a.ws_dt = reinterpret_cast<float*>(ws);
   ws += up(p->nchunks * p->nheads * p->chunk_size * 4);
   a.ws_acum = reinterpret_cast<float*>(ws);
-  ws += up(p->nchunks * p->nheads * p->chunk_size * 4);
-  a.ws_cb = reinterpret_cast<float*>(ws);
+  a.err = ssu::device_error_word();
+  if (!a.err) return bad(SSU_ERR_CUDA, "device error word unavailable");
   cudaError_t e;
   const cudaStream_t s = (cudaStream_t)stream;
   if (p->io_dtype == SSU_BF16)

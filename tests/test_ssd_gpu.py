@@ -74,6 +74,7 @@ def close(got, ref, label):
 
 def parity(o, c, label, **kw):
     out, states = run_gpu(c, **kw)
+    assert ssu.ssu_device_error() == 0, "a tensor-core wait gave up"
     y_ref, s_ref = run_oracle(o, c.to("cpu"), **kw)
     covered = int(c.cu_chunk_seqlens[-1])
     ry = close(out[:covered], y_ref[:covered], f"{label}: y")
@@ -175,3 +176,24 @@ def test_ssd_out_in_place_and_untouched_tokens():
     assert bool((out[T - 10:] == 7.0).all())
     assert bool(torch.isfinite(out[:T - 10].float()).all())
     assert tuple(st.shape) == (2, 4, 64, 64)
+
+
+def test_ssd_call_is_three_launches():
+    """Chunk states, state passing and the scan (which forms C . B^T itself):
+    three kernels per call, whatever the batch, and no allocation with out,
+    states and workspace given."""
+    from ._parity import graph_kernel_nodes
+    c = W.ssd_case(lengths=[300, 17, 256], heads=8, headdim=64, dstate=128, groups=2,
+                   chunk_size=128, seed=11, device=DEV)
+    out = torch.empty_like(c.x)
+    nch = c.cu_chunk_seqlens.numel() - 1
+    states = torch.empty((3, 8, 64, 128), dtype=torch.float32, device=DEV)
+    ws = torch.empty(ssu.ssd_workspace_bytes(nch, 8, 2, 64, 128, 128), dtype=torch.uint8,
+                     device=DEV)
+
+    def call():
+        ssu.ssd_combined_fwd_varlen(c.x, c.dt, c.A, c.B, c.C, c.chunk_size, c.cu_seqlens,
+                                    c.cu_chunk_seqlens, c.last_chunk_indices, c.seq_idx, out=out,
+                                    D=c.D, z=c.z, dt_bias=c.dt_bias, dt_softplus=True,
+                                    initial_states=c.initial_states, states=states, workspace=ws)
+    assert graph_kernel_nodes(call) == 3
