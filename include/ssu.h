@@ -414,6 +414,7 @@ ssu_status ssu_replay_update_static(const ssu_params* p, const ssu_replay_cache*
  *                 last_chunk_indices [batch]: sequence b's last chunk.  All
  *                 meta_dtype (I32 / I64).
  *   initial_states [batch, nheads, headdim, dstate] in initial_dtype, or NULL
+ *                 (16-byte aligned, like states)
  *   states        return_intermediate_states: [nchunks, nheads, headdim,
  *                 dstate], every chunk's end state; else [batch, ...], the
  *                 end state of each sequence's last chunk (chunk c is

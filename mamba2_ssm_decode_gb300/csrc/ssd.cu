@@ -255,8 +255,8 @@ __global__ void __launch_bounds__(128) ssd_chunk_state_kernel(const SSDArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// 2. state passing: sequential over chunks, four state values per thread.
-//    One CTA covers 512 values of one head; per block of chunks the CTA first
+// 2. state passing: sequential over chunks, eight state values per thread.
+//    One CTA covers 1024 values of one head; per block of chunks the CTA first
 //    tabulates each chunk's decay exp(a_{L-1}), whether it opens a sequence
 //    and where its end state goes, so that the loop itself only multiplies,
 //    adds and streams the chunk states (loaded several chunks ahead).  Each
@@ -289,19 +289,63 @@ __device__ __forceinline__ void split_packed<__half>(float a, float b, uint32_t*
   *lo = *reinterpret_cast<const uint32_t*>(&l2);
 }
 
+// 8 consecutive values at element offset `o` (a multiple of 8) of an fp32,
+// bf16 or fp16 array (16-byte aligned), as floats / from floats (RNE)
+__device__ __forceinline__ void load8(const void* p, int64_t o, int dtype, float (&v)[8]) {
+  if (dtype == 0) {
+    const float4 a = reinterpret_cast<const float4*>(static_cast<const float*>(p) + o)[0];
+    const float4 b = reinterpret_cast<const float4*>(static_cast<const float*>(p) + o)[1];
+    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+    return;
+  }
+  const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const char*>(p) + o * 2);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (dtype == 1) {
+      v[2 * k] = __uint_as_float(w[k] << 16);
+      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    } else {
+      const __half2 h2 = *reinterpret_cast<const __half2*>(&w[k]);
+      v[2 * k] = __low2float(h2);
+      v[2 * k + 1] = __high2float(h2);
+    }
+  }
+}
+
+__device__ __forceinline__ void store8(void* p, int64_t o, int dtype, const float (&v)[8]) {
+  if (dtype == 0) {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(p) + o);
+    d[0] = make_float4(v[0], v[1], v[2], v[3]);
+    d[1] = make_float4(v[4], v[5], v[6], v[7]);
+    return;
+  }
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    w[k] = dtype == 1 ? pack_pair<__nv_bfloat16>(v[2 * k], v[2 * k + 1])
+                      : pack_pair<__half>(v[2 * k], v[2 * k + 1]);
+  *reinterpret_cast<uint4*>(static_cast<char*>(p) + o * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One CTA covers 1024 values of one head: kPassRows = 1024 / N rows p, all N
+// columns; thread (pl, ng) owns row p = kPassRows blockIdx.x + pl, columns
+// [8 ng, 8 ng + 8), so that the threads of a warp write whole 16-byte core-
+// matrix rows of the operand layout next to each other.
 template <class IT, int P, int N>
 __global__ void __launch_bounds__(128) ssd_state_passing_kernel(const SSDArgs a) {
+  constexpr int kRows = 1024 / N;
+  static_assert(P % kRows == 0, "whole CTAs per head");
   __shared__ float s_decay[kPassBlock];
   __shared__ int64_t s_seq[kPassBlock];
   __shared__ int64_t s_dst[kPassBlock];  // destination row of the end state, or -1
   const int64_t HPN = (int64_t)a.H * P * N;
-  const int64_t e = ((int64_t)blockIdx.x * 128 + threadIdx.x) * 4;  // < HPN (exact grid)
-  const int h = (int)(((int64_t)blockIdx.x * 512) / (P * N));
-  // this thread's 4 values: (p, n .. n + 3) of head h; their 8-byte slot in
-  // the operand layout of ws_henter
-  const int el = (int)(e - (int64_t)h * P * N), pp = el / N, nn = el - pp * N;
-  const uint32_t hoff = (uint32_t)((nn >> 3) * (P * 16) + pp * 16 + (nn & 7) * 2);
-  float4 hc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  const int h = blockIdx.x / (P / kRows);
+  const int pl = threadIdx.x % kRows, ng = threadIdx.x / kRows;
+  const int pp = (blockIdx.x % (P / kRows)) * kRows + pl;
+  const int64_t e = (int64_t)h * P * N + (int64_t)pp * N + ng * 8;  // first of this thread's 8
+  const uint32_t hoff = (uint32_t)(ng * (P * 16) + pp * 16);         // its 16-byte operand row
+  float hc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   int64_t prev = -1;
   for (int cb = 0; cb < a.nchunks; cb += kPassBlock) {
     const int nb = min(kPassBlock, a.nchunks - cb);
@@ -321,41 +365,44 @@ __global__ void __launch_bounds__(128) ssd_state_passing_kernel(const SSDArgs a)
     }
     __syncthreads();
     const float4* wsp = reinterpret_cast<const float4*>(a.ws_state + (int64_t)cb * HPN + e);
-    float4 buf[kPassAhead];
+    float4 buf[kPassAhead][2];  // chunk states in flight, kPassAhead chunks ahead
 #pragma unroll
     for (int k = 0; k < kPassAhead; ++k)
-      if (k < nb) buf[k] = wsp[(int64_t)k * (HPN / 4)];
-    for (int i = 0; i < nb; ++i) {
-      const float4 S = buf[i % kPassAhead];
-      if (i + kPassAhead < nb) buf[i % kPassAhead] = wsp[(int64_t)(i + kPassAhead) * (HPN / 4)];
-      const int64_t sq = s_seq[i];
-      if (cb + i == 0 || sq != prev) {  // the chunk opens sequence sq
-        hc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (a.init && sq >= 0 && sq < a.batch) {
-          const int64_t o = sq * HPN + e;
-          hc = make_float4(load_f(a.init, o, a.init_dtype), load_f(a.init, o + 1, a.init_dtype),
-                           load_f(a.init, o + 2, a.init_dtype),
-                           load_f(a.init, o + 3, a.init_dtype));
+      if (k < nb) {
+        buf[k][0] = wsp[(int64_t)k * (HPN / 4)];
+        buf[k][1] = wsp[(int64_t)k * (HPN / 4) + 1];
+      }
+    for (int i0 = 0; i0 < nb; i0 += kPassAhead) {
+#pragma unroll
+      for (int u = 0; u < kPassAhead; ++u) {
+        const int i = i0 + u;
+        if (i >= nb) break;
+        const float S[8] = {buf[u][0].x, buf[u][0].y, buf[u][0].z, buf[u][0].w,
+                            buf[u][1].x, buf[u][1].y, buf[u][1].z, buf[u][1].w};
+        if (i + kPassAhead < nb) {
+          buf[u][0] = wsp[(int64_t)(i + kPassAhead) * (HPN / 4)];
+          buf[u][1] = wsp[(int64_t)(i + kPassAhead) * (HPN / 4) + 1];
         }
-      }
-      prev = sq;
-      {  // the entering state, for the scan
-        uint8_t* blk = a.ws_henter + ((int64_t)(cb + i) * a.H + h) * (P * N * 4);
-        uint32_t h0, h1, l0, l1;
-        split_packed<IT>(hc.x, hc.y, &h0, &l0);
-        split_packed<IT>(hc.z, hc.w, &h1, &l1);
-        *reinterpret_cast<uint2*>(blk + hoff) = make_uint2(h0, h1);
-        *reinterpret_cast<uint2*>(blk + P * N * 2 + hoff) = make_uint2(l0, l1);
-      }
-      const float d = s_decay[i];
-      hc = make_float4(d * hc.x + S.x, d * hc.y + S.y, d * hc.z + S.z, d * hc.w + S.w);
-      const int64_t dst = s_dst[i];
-      if (dst >= 0) {
-        const int64_t o = dst * HPN + e;
-        store_f(a.states, o, a.state_dtype, hc.x);
-        store_f(a.states, o + 1, a.state_dtype, hc.y);
-        store_f(a.states, o + 2, a.state_dtype, hc.z);
-        store_f(a.states, o + 3, a.state_dtype, hc.w);
+        const int64_t sq = s_seq[i];
+        if (cb + i == 0 || sq != prev) {  // the chunk opens sequence sq
+#pragma unroll
+          for (int k = 0; k < 8; ++k) hc[k] = 0.0f;
+          if (a.init && sq >= 0 && sq < a.batch) load8(a.init, sq * HPN + e, a.init_dtype, hc);
+        }
+        prev = sq;
+        {  // the entering state, for the scan
+          uint8_t* blk = a.ws_henter + ((int64_t)(cb + i) * a.H + h) * (P * N * 4);
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) split_packed<IT>(hc[2 * k], hc[2 * k + 1], &hi[k], &lo[k]);
+          *reinterpret_cast<uint4*>(blk + hoff) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(blk + P * N * 2 + hoff) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        const float d = s_decay[i];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) hc[k] = d * hc[k] + S[k];
+        const int64_t dst = s_dst[i];
+        if (dst >= 0) store8(a.states, dst * HPN + e, a.state_dtype, hc);
       }
     }
   }
@@ -697,9 +744,9 @@ cudaError_t launch(const SSDArgs& a, cudaStream_t stream) {
   ssd_chunk_state_kernel<IT, P, N><<<dim3(a.nchunks, a.H), 128, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  static_assert((P * N) % 512 == 0, "a state-passing CTA covers 512 values of one head");
+  static_assert((P * N) % 1024 == 0, "a state-passing CTA covers 1024 values of one head");
   ssd_state_passing_kernel<IT, P, N>
-      <<<(unsigned)((int64_t)a.H * P * N / 512), 128, 0, stream>>>(a);
+      <<<(unsigned)((int64_t)a.H * P * N / 1024), 128, 0, stream>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto scan = ssd_chunk_scan_kernel<IT, P, N>;
   const int smem = (int)sizeof(ScanSmem<P, N>) > kScanMinSmem ? (int)sizeof(ScanSmem<P, N>)
@@ -772,8 +819,10 @@ ssu_status ssd_combined_fwd_varlen(const ssd_params* p, void* workspace, int64_t
   if (!p->x || !p->dt || !p->A || !p->B || !p->C || !p->out || !p->states ||
       !p->cu_chunk_seqlens || !p->seq_idx || (!p->return_intermediate_states && !p->last_chunk_indices))
     return bad(SSU_ERR_INVALID_ARGUMENT, "x, dt, A, B, C, out, states and the chunk metadata must not be NULL");
-  if (!a16(p->x) || !a16(p->B) || !a16(p->C) || !a16(p->out) || (p->z && !a16(p->z)))
-    return bad(SSU_ERR_INVALID_ARGUMENT, "x, z, out, B and C must be 16-byte aligned");
+  if (!a16(p->x) || !a16(p->B) || !a16(p->C) || !a16(p->out) || (p->z && !a16(p->z)) ||
+      !a16(p->states) || (p->initial_states && !a16(p->initial_states)))
+    return bad(SSU_ERR_INVALID_ARGUMENT,
+               "x, z, out, B, C, states and initial_states must be 16-byte aligned");
   if (!(p->dt_min <= p->dt_max)) return bad(SSU_ERR_INVALID_ARGUMENT, "dt_limit must be (lo, hi) with lo <= hi");
   const int64_t need = ssd::workspace_bytes(p->nchunks, p->nheads, p->ngroups, p->headdim,
                                             p->dstate, p->chunk_size);
