@@ -12,13 +12,13 @@
 //   bmm          CB[t,s] = C_t . B_s
 //   chunk_scan   y_t    = sum_{s<=t} CB[t,s] exp(a_t - a_s) dt'_s x_s
 //                         + exp(a_t) C_t . h_enter + D x_t     (times silu(z_t))
-// Three launches on the caller's stream: (1) dt', a_t and S per chunk and head
-// (cumsum + chunk_state, warp-level m16n8k16 MMAs); (2) the sequential state
-// passing, which also stores each chunk's entering state in the tensor-core
-// operand layout; (3) the scan on the fifth-generation tensor cores (tcgen05:
-// fp32 accumulators in tensor memory), which forms C . B^T itself (the bmm
-// stage) 64 source tokens at a time and feeds it, decayed and masked, straight
-// back into the intra-chunk product.  The inputs x, B, C are 16-bit already;
+// Three launches on the caller's stream, the contractions on the fifth-
+// generation tensor cores (tcgen05: MMAs issued by one thread, fp32
+// accumulators in tensor memory): (1) dt', a_t and S per chunk and pair of
+// heads (cumsum + chunk_state); (2) the sequential state passing, which also
+// stores each chunk's entering state in the tensor-core operand layout; (3)
+// the scan, which forms C . B^T itself (the bmm stage), 128 source tokens at
+// a time, and feeds it, decayed and masked, back into the intra-chunk product.  The inputs x, B, C are 16-bit already;
 // an operand the kernels compute (w_s x_s, the decayed C . B^T, h_enter) is
 // split into a 16-bit high part and a 16-bit remainder and multiplied twice,
 // so that it enters the products to about 2^-16 instead of 2^-8 (the outputs
@@ -73,45 +73,6 @@ struct SSDArgs {
   unsigned* err;        // device error word
 };
 
-// v = hi + lo with hi, lo in the io dtype (lo: the rounding remainder of hi)
-template <class IT>
-__device__ __forceinline__ void split2(float v, IT* hi, IT* lo) {
-  *hi = float_to_io<IT>(v);
-  *lo = float_to_io<IT>(v - io_to_float<IT>(*hi));
-}
-
-// packed (low, high) pairs of the high parts and of the remainders of (a, b)
-template <class IT>
-__device__ __forceinline__ void split_pair(float a, float b, uint32_t* hi, uint32_t* lo) {
-  IT ah, al, bh, bl;
-  split2<IT>(a, &ah, &al);
-  split2<IT>(b, &bh, &bl);
-  *hi = pack_pair<IT>(io_to_float<IT>(ah), io_to_float<IT>(bh));
-  *lo = pack_pair<IT>(io_to_float<IT>(al), io_to_float<IT>(bl));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&a)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ uint32_t saddr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ float load_f(const void* p, int64_t i, int dtype) {
-  if (dtype == 0) return static_cast<const float*>(p)[i];
-  if (dtype == 1) return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
-  return __half2float(static_cast<const __half*>(p)[i]);
-}
-
-__device__ __forceinline__ void store_f(void* p, int64_t i, int dtype, float v) {
-  if (dtype == 0) static_cast<float*>(p)[i] = v;
-  else if (dtype == 1) static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
-  else static_cast<__half*>(p)[i] = __float2half_rn(v);
-}
-
 // tokens [t0, t0 + Lc) of chunk c (Lc clamped to [0, CS])
 __device__ __forceinline__ void chunk_span(const SSDArgs& a, int c, int64_t* t0, int* Lc) {
   const int64_t b = load_int(a.cu_chunk, c, a.meta64);
@@ -123,150 +84,6 @@ __device__ __forceinline__ void chunk_span(const SSDArgs& a, int c, int64_t* t0,
   *t0 = b;
   *Lc = (int)n;
 }
-
-// 8 consecutive 16-bit values from global memory into shared (16-byte aligned)
-template <class IT>
-__device__ __forceinline__ void copy8(IT* dst, const IT* src) {
-  *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
-}
-
-// ---------------------------------------------------------------------------
-// 1. dt', a_t and the chunk-local state S (one CTA per chunk and head)
-// ---------------------------------------------------------------------------
-template <class IT, int P, int N>
-__global__ void __launch_bounds__(128) ssd_chunk_state_kernel(const SSDArgs a) {
-  constexpr int KB = 32;  // tokens per staged block
-  const int c = blockIdx.x, h = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ float s_dtp[kMaxChunk], s_acum[kMaxChunk], s_w[kMaxChunk];
-  __shared__ __align__(16) IT Xs[2][KB][P + 8];  // w_s x_s: high parts, remainders
-  __shared__ __align__(16) IT Bs[KB][N + 8];
-  int64_t t0;
-  int Lc;
-  chunk_span(a, c, &t0, &Lc);
-  const int g = h / a.hr;
-  const float Ah = a.A[h];
-  const float bias = a.dt_bias ? a.dt_bias[h] : 0.0f;
-  for (int i = tid; i < kMaxChunk; i += 128) {
-    float d = 0.0f;
-    if (i < Lc) {
-      d = a.dt[(t0 + i) * a.H + h] + bias;
-      if (a.softplus) d = softplus_f(d);
-      d = fminf(fmaxf(d, a.dt_lo), a.dt_hi);
-    }
-    s_dtp[i] = d;
-    s_acum[i] = Ah * d;
-  }
-  __syncthreads();
-  // inclusive running sum over the chunk: warp 0, eight values per lane
-  if (warp == 0) {
-    float v[8], run = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      run += s_acum[lane * 8 + k];
-      v[k] = run;
-    }
-    float incl = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float u = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += u;
-    }
-    const float before = incl - run;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) s_acum[lane * 8 + k] = v[k] + before;
-  }
-  __syncthreads();
-  const float a_end = Lc > 0 ? s_acum[Lc - 1] : 0.0f;
-  float* wdt = a.ws_dt + ((int64_t)c * a.H + h) * a.CS;
-  float* wac = a.ws_acum + ((int64_t)c * a.H + h) * a.CS;
-  for (int i = tid; i < Lc; i += 128) {
-    wdt[i] = s_dtp[i];
-    wac[i] = s_acum[i];
-    s_w[i] = expf(a_end - s_acum[i]) * s_dtp[i];
-  }
-  __syncthreads();
-
-  // S[p][n] = sum_s w_s x_s[p] B_s[n]: M = P (p), N = N (n), K = tokens.
-  // Warp w owns p rows [16 w, 16 w + 16).
-  constexpr int NT = N / 8;
-  float acc[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
-  const IT* xg = static_cast<const IT*>(a.x);
-  const IT* bg = static_cast<const IT*>(a.B);
-  for (int k0 = 0; k0 < Lc; k0 += KB) {
-    // stage w_s x_s (rounded to the io dtype) and B_s, zero past the chunk
-    for (int i = tid; i < KB * (P / 8); i += 128) {
-      const int r = i / (P / 8), q8 = (i - r * (P / 8)) * 8;
-      const int s = k0 + r;
-      if (s < Lc) {
-        uint4 raw = __ldg(reinterpret_cast<const uint4*>(xg + ((t0 + s) * a.H + h) * P + q8));
-        const IT* e = reinterpret_cast<const IT*>(&raw);
-        const float w = s_w[s];
-        __align__(16) IT hi[8];
-        __align__(16) IT lo[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) split2<IT>(w * io_to_float<IT>(e[k]), &hi[k], &lo[k]);
-        *reinterpret_cast<uint4*>(&Xs[0][r][q8]) = *reinterpret_cast<const uint4*>(hi);
-        *reinterpret_cast<uint4*>(&Xs[1][r][q8]) = *reinterpret_cast<const uint4*>(lo);
-      } else {
-        *reinterpret_cast<uint4*>(&Xs[0][r][q8]) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(&Xs[1][r][q8]) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    for (int i = tid; i < KB * (N / 8); i += 128) {
-      const int r = i / (N / 8), q8 = (i - r * (N / 8)) * 8;
-      const int s = k0 + r;
-      if (s < Lc) copy8(&Bs[r][q8], bg + ((t0 + s) * a.G + g) * N + q8);
-      else *reinterpret_cast<uint4*>(&Bs[r][q8]) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    __syncthreads();
-    if (warp * 16 < P) {
-#pragma unroll
-      for (int ks = 0; ks < KB / 16; ++ks) {
-        const int m = lane >> 3, j = lane & 7;
-        uint32_t ah[4], al[4];  // A = (w x)^T: rows p, columns s (stored [s][p])
-        ldsm_x4_t(ah, saddr(&Xs[0][ks * 16 + j + (m >= 2 ? 8 : 0)][warp * 16 + (m & 1 ? 8 : 0)]));
-        ldsm_x4_t(al, saddr(&Xs[1][ks * 16 + j + (m >= 2 ? 8 : 0)][warp * 16 + (m & 1 ? 8 : 0)]));
-#pragma unroll
-        for (int np = 0; np < NT / 2; ++np) {
-          uint32_t bf[4];  // B: rows s, columns n (stored [s][n]: transposed loads)
-          ldsm_x4_t(bf, saddr(&Bs[ks * 16 + j + (m & 1 ? 8 : 0)][np * 16 + (m >= 2 ? 8 : 0)]));
-          mma_16816<IT>(acc[2 * np], ah, bf[0], bf[1]);
-          mma_16816<IT>(acc[2 * np + 1], ah, bf[2], bf[3]);
-          mma_16816<IT>(acc[2 * np], al, bf[0], bf[1]);
-          mma_16816<IT>(acc[2 * np + 1], al, bf[2], bf[3]);
-        }
-      }
-    }
-    __syncthreads();
-  }
-  if (warp * 16 < P) {
-    float* out = a.ws_state + ((int64_t)c * a.H + h) * P * N;
-    const int r0 = warp * 16 + (lane >> 2), c0 = 2 * (lane & 3);
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      *reinterpret_cast<float2*>(&out[r0 * N + j * 8 + c0]) = make_float2(acc[j][0], acc[j][1]);
-      *reinterpret_cast<float2*>(&out[(r0 + 8) * N + j * 8 + c0]) =
-          make_float2(acc[j][2], acc[j][3]);
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// 2. state passing: sequential over chunks, eight state values per thread.
-//    One CTA covers 1024 values of one head; per block of chunks the CTA first
-//    tabulates each chunk's decay exp(a_{L-1}), whether it opens a sequence
-//    and where its end state goes, so that the loop itself only multiplies,
-//    adds and streams the chunk states (loaded several chunks ahead).  Each
-//    chunk's entering state goes to ws_henter as 16-bit high parts and
-//    remainders, laid out as the scan's B operand of C . h_enter^T: a K-major
-//    [P rows (p)] x [N (n)] tile whose 16-byte core-matrix rows (8 n of one p)
-//    sit at (n / 8) * 16 P + 16 p, high parts first, remainders P N 2 bytes on.
-// ---------------------------------------------------------------------------
-constexpr int kPassBlock = 256;  // chunks tabulated at a time
-constexpr int kPassAhead = 4;    // chunk states in flight per thread
 
 // hi + lo = (a, b) to 16-bit precision each: packed (low = a, high = b) pairs
 template <class IT>
@@ -288,6 +105,228 @@ __device__ __forceinline__ void split_packed<__half>(float a, float b, uint32_t*
   *hi = *reinterpret_cast<const uint32_t*>(&h2);
   *lo = *reinterpret_cast<const uint32_t*>(&l2);
 }
+
+// Spin on an mbarrier phase (the tensor core finishes within microseconds: a
+// suspended wait would add its wake-up latency); false after `limit_ns`.
+__device__ __forceinline__ bool spin_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 1. dt', a_t and the chunk-local state S on the fifth-generation tensor
+//    cores: one CTA of 256 threads per chunk and pair of heads of one group
+//    (one head when the groups have an odd number of heads).  With
+//    w_{k,s} = exp(a_end - a_s) dt'_s for head k,
+//      S_k[p][n] = sum_s (w_{k,s} x_{k,s}[p]) B_s[n]
+//    is one M = 128 (two heads x 64 p) x N (dstate) MMA chain over the
+//    chunk's tokens, 64 at a time (K = tokens).  Both operands are MN-major,
+//    so x and B rows keep their global layout: 16-byte pieces (8 p, or 8 n,
+//    of one token) sit at (p / 8 or n / 8) 1024 + 16 s (LBO 128, SBO 1024).
+//    The A operand w x is computed, so it is split into high parts and
+//    remainders (two MMAs per step); B rows are copied in by cp.async one
+//    slice ahead.
+// ---------------------------------------------------------------------------
+constexpr int kStSL = 64;  // tokens per slice
+
+template <int N>
+struct StateSmem {
+  uint8_t as[2][128 * kStSL * 2];  // w x of the slice: high parts, remainders
+  uint8_t bs[2][N * kStSL * 2];    // B rows of a slice, two buffers
+  float w[2][kMaxChunk];           // per head: a_t, then w_t
+  uint64_t bar;
+  uint32_t tmem;
+};
+
+template <class IT, int P, int N>
+__global__ void __launch_bounds__(256) ssd_chunk_state_kernel(const SSDArgs a) {
+  static_assert(P == 64 && (N == 64 || N == 128), "headdim 64, dstate 64 or 128");
+  constexpr bool kBF16 = std::is_same<IT, __nv_bfloat16>::value;
+  constexpr uint32_t kId = tc::idesc_f16(kBF16, 128, N, true, true);
+  constexpr uint32_t kCols = N;  // 64 or 128 fp32 columns
+  constexpr int NT = 256;
+  const int c = blockIdx.x;
+  const bool pair = (a.hr % 2) == 0;
+  const int h0 = pair ? 2 * blockIdx.y : blockIdx.y, nh = pair ? 2 : 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  auto& sm = *reinterpret_cast<StateSmem<N>*>(smem_raw);
+  int64_t t0;
+  int Lc;
+  chunk_span(a, c, &t0, &Lc);
+  if (*reinterpret_cast<volatile unsigned*>(a.err) & kErrMmaTimeout) return;  // a wait gave up
+  if (Lc == 0) {  // an empty chunk: S = 0
+    for (int i = tid; i < nh * P * N / 4; i += NT)
+      reinterpret_cast<float4*>(a.ws_state + ((int64_t)c * a.H + h0) * P * N)[i] =
+          make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const int g = h0 / a.hr;
+  const IT* bg = static_cast<const IT*>(a.B);
+  const IT* xg = static_cast<const IT*>(a.x);
+  const uint32_t s_as[2] = {smem_addr(sm.as[0]), smem_addr(sm.as[1])};
+  const uint32_t s_bs[2] = {smem_addr(sm.bs[0]), smem_addr(sm.bs[1])};
+  auto load_b = [&](int j) {
+#pragma unroll 1
+    for (int q = tid; q < kStSL * (N / 8); q += NT) {
+      const int sl = q % kStSL, ng = q / kStSL, s = j * kStSL + sl;
+      const bool ok = s < Lc;
+      tc::cp16(s_bs[j & 1] + ng * 1024 + sl * 16, bg + ((t0 + (ok ? s : 0)) * a.G + g) * N + ng * 8,
+               ok ? 16u : 0u);
+    }
+  };
+  load_b(0);
+  tc::cp_commit();
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tc::alloc(smem_addr(&sm.tmem), kCols);
+  // dt', a_t (inclusive running sum of A dt') and w_t per head: warp k takes
+  // head h0 + k, eight tokens per lane
+  if (warp < nh) {
+    const int h = h0 + warp;
+    const float Ah = a.A[h];
+    const float bias = a.dt_bias ? a.dt_bias[h] : 0.0f;
+    float d[8], v[8], run = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = lane * 8 + k;
+      float x = 0.0f;
+      if (i < Lc) {
+        x = a.dt[(t0 + i) * a.H + h] + bias;
+        if (a.softplus) x = softplus_f(x);
+        x = fminf(fmaxf(x, a.dt_lo), a.dt_hi);
+      }
+      d[k] = x;
+      run += Ah * x;
+      v[k] = run;
+    }
+    float incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    const float before = incl - run;
+    float* wdt = a.ws_dt + ((int64_t)c * a.H + h) * a.CS;
+    float* wac = a.ws_acum + ((int64_t)c * a.H + h) * a.CS;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = lane * 8 + k;
+      v[k] += before;
+      sm.w[warp][i] = v[k];
+      if (i < Lc) {
+        wdt[i] = d[k];
+        wac[i] = v[k];
+      }
+    }
+    __syncwarp();
+    const float a_end = sm.w[warp][Lc - 1];
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = lane * 8 + k;
+      sm.w[warp][i] = i < Lc ? expf(a_end - v[k]) * d[k] : 0.0f;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sm.tmem;
+  bool dead = false;
+  auto wait = [&](uint32_t parity) {
+    if (!dead && !spin_wait(&sm.bar, parity, kWaitLimitNs)) {
+      dead = true;
+      atomicOr(a.err, kErrMmaTimeout);
+    }
+  };
+  const int J = (Lc + kStSL - 1) / kStSL;
+  uint32_t ph = 0;
+  for (int j = 0; j < J; ++j) {
+    if (j > 0) {  // the previous MMAs are done: the A buffer and B buffer (j + 1) % 2 are free
+      wait(ph);
+      ph ^= 1;
+    }
+    if (j + 1 < J) load_b(j + 1);
+    tc::cp_commit();
+    // w x of the slice, 8 p of one token per 16-byte piece, split
+#pragma unroll 1
+    for (int q = tid; q < 2 * kStSL * (P / 8); q += NT) {
+      const int k = q / (kStSL * (P / 8)), rem = q % (kStSL * (P / 8));
+      const int sl = rem % kStSL, pg = rem / kStSL, s = j * kStSL + sl;
+      uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = make_uint4(0u, 0u, 0u, 0u);
+      if (k < nh && s < Lc) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(xg + ((t0 + s) * a.H + h0 + k) * P + pg * 8));
+        const IT* e = reinterpret_cast<const IT*>(&raw);
+        const float ws = sm.w[k][s];
+        uint32_t hp[4], lp[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          split_packed<IT>(ws * io_to_float<IT>(e[2 * u]), ws * io_to_float<IT>(e[2 * u + 1]), &hp[u],
+                           &lp[u]);
+        hi = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+        lo = make_uint4(lp[0], lp[1], lp[2], lp[3]);
+      }
+      const int off = (k * 8 + pg) * 1024 + sl * 16;
+      *reinterpret_cast<uint4*>(sm.as[0] + off) = hi;
+      *reinterpret_cast<uint4*>(sm.as[1] + off) = lo;
+    }
+    tc::cp_wait<1>();  // all but the newest group: B_j has landed
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid == 0) {
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int kk = 0; kk < kStSL / 16; ++kk)
+          tc::mma(tmem, tc::sdesc(s_as[part] + kk * 256, 128, 1024),
+                  tc::sdesc(s_bs[j & 1] + kk * 256, 128, 1024), kId, (j | part | kk) != 0);
+      tc::commit(smem_addr(&sm.bar));
+    }
+  }
+  wait(ph);  // the last MMAs are done: S is final
+  tc::fence_after_sync();
+  // row m = 32 (warp % 4) + lane is (head m / 64, p m % 64); warpgroup
+  // warp / 4 stores columns [N/2 (warp / 4), N/2 (warp / 4) + N/2)
+  const int m = 32 * (warp & 3) + lane, k = m / P, pp = m % P, wg = warp >> 2;
+  float* dst = a.ws_state + (((int64_t)c * a.H + h0 + k) * P + pp) * N + wg * (N / 2);
+#pragma unroll 1
+  for (int c16 = 0; c16 < N / 32; ++c16) {
+    float v[16];
+    tc::ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + wg * (N / 2) + c16 * 16, v);
+    tc::wait_ld();
+    if (k < nh) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        reinterpret_cast<float4*>(dst + c16 * 16)[u] =
+            make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tmem, kCols);
+}
+
+// ---------------------------------------------------------------------------
+// 2. state passing: sequential over chunks, eight state values per thread.
+//    One CTA covers 1024 values of one head; per block of chunks the CTA first
+//    tabulates each chunk's decay exp(a_{L-1}), whether it opens a sequence
+//    and where its end state goes, so that the loop itself only multiplies,
+//    adds and streams the chunk states (loaded several chunks ahead).  Each
+//    chunk's entering state goes to ws_henter as 16-bit high parts and
+//    remainders, laid out as the scan's B operand of C . h_enter^T: a K-major
+//    [P rows (p)] x [N (n)] tile whose 16-byte core-matrix rows (8 n of one p)
+//    sit at (n / 8) * 16 P + 16 p, high parts first, remainders P N 2 bytes on.
+// ---------------------------------------------------------------------------
+constexpr int kPassBlock = 256;  // chunks tabulated at a time
+constexpr int kPassAhead = 4;    // chunk states in flight per thread
 
 // 8 consecutive values at element offset `o` (a multiple of 8) of an fp32,
 // bf16 or fp16 array (16-byte aligned), as floats / from floats (RNE)
@@ -456,17 +495,6 @@ struct ScanSmem {
   uint64_t bar_h, bar_cb, bar_intra;
   uint32_t tmem;
 };
-
-// Spin on an mbarrier phase (the tensor core finishes within microseconds: a
-// suspended wait would add its wake-up latency); false after `limit_ns`.
-__device__ __forceinline__ bool spin_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_test(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_test(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
-  }
-}
 
 template <class IT, int P, int N>
 __global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
@@ -741,9 +769,14 @@ __global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
 
 template <class IT, int P, int N>
 cudaError_t launch(const SSDArgs& a, cudaStream_t stream) {
-  ssd_chunk_state_kernel<IT, P, N><<<dim3(a.nchunks, a.H), 128, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  auto state = ssd_chunk_state_kernel<IT, P, N>;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sizeof(StateSmem<N>))) != cudaSuccess)
+    return e;
+  const unsigned pairs = (a.hr % 2 == 0) ? (unsigned)(a.H / 2) : (unsigned)a.H;
+  state<<<dim3(a.nchunks, pairs), 256, sizeof(StateSmem<N>), stream>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   static_assert((P * N) % 1024 == 0, "a state-passing CTA covers 1024 values of one head");
   ssd_state_passing_kernel<IT, P, N>
       <<<(unsigned)((int64_t)a.H * P * N / 1024), 128, 0, stream>>>(a);
