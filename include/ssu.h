@@ -86,7 +86,9 @@ typedef enum ssu_status {
  *                    copy while consumer warps compute
  * For calls that write state both compute the same arithmetic in the same
  * order (bit-identical results); for calls that write none the closed form
- * rounds differently (within the same tolerances).
+ * rounds differently (within the same tolerances).  Calls with stochastic
+ * rounding of 16-bit state (rand_seed set) run on the DIRECT kernels
+ * whatever the choice: only those carry the generator.
  */
 typedef enum ssu_algorithm {
   SSU_ALGO_AUTO = 0,

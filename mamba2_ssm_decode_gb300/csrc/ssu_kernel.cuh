@@ -431,19 +431,17 @@ __device__ __forceinline__ uint32_t sr_f16(float v, uint32_t r) {
 }
 
 // Store 8 (16-bit state) or 4 (fp32) consecutive state values h (pairs) at
-// element `off` of the pool: to nearest even, or -- 16-bit state with a seed
-// -- stochastically, element e taking the 16 bits 16 (e mod 4) of word
-// (e / 4) mod 4 of Philox block e / 16 keyed by (seed, 0).
-template <class ST>
+// element `off` of the pool: to nearest even, or -- 16-bit state, in the
+// kernels instantiated with SR -- stochastically, element e taking the 16
+// bits 16 (e mod 4) of word (e / 4) mod 4 of Philox block e / 16 keyed by
+// (seed, 0).  The generator lives only in the SR instantiations, so the
+// round-to-nearest kernels keep their code size and registers.
+template <class ST, bool SR = false>
 __device__ __forceinline__ void store_state(ST* state, int64_t off, const float2* h,
                                             const KParams& p) {
-  if constexpr (sizeof(ST) == 4) {
+  if constexpr (sizeof(ST) == 4 || !SR) {
     st_state(state + off, Elem<ST>::pack2(h));
   } else {
-    if (!p.sr_seed) {
-      st_state(state + off, Elem<ST>::pack2(h));
-      return;
-    }
     uint64_t x[4] = {(uint64_t)off >> 4, 0, 0, 0};
     philox4x64(x, __ldg(p.sr_seed), 0, p.sr_rounds);
     const bool upper = ((uint64_t)off >> 3) & 1;  // the chunk is half a block
@@ -537,7 +535,8 @@ __device__ __forceinline__ void stage_steps(Stage<N, ROWS, LMAX>& s, const KPara
 // One CTA: rows [p0, p0 + ROWS) of head h, sequence rows [r0, r0 + len),
 // state read from `src` (if read_ok), step t written to dst_of(t).
 // (with the stage in caller-provided shared memory)
-template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, class DstFn, class StageT>
+template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, bool SR, class DstFn,
+          class StageT>
 __device__ __forceinline__ void ssu_block_on(StageT& stg, const KParams& p, int h, int p0,
                                              int64_t r0, int len, int64_t src, bool read_ok,
                                              DstFn dst_of) {
@@ -612,7 +611,7 @@ __device__ __forceinline__ void ssu_block_on(StageT& stg, const KParams& p, int 
           if (prow < p.P) {
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c)
-              store_state<ST>(state, base - state + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
+              store_state<ST, SR>(state, base - state + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
                               &hs[u][c * L::VEC / 2], p);
           }
         }

@@ -168,7 +168,10 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
   // auto (the fastest as measured): the bulk-copy pipeline for one-token calls
   // that write state, the head-run kernels for every other call
   const bool auto_bulk = !varlen && !p.disable;
-  const bool bulk = algorithm == 2 /* SSU_ALGO_BULK */ || (algorithm == 0 && auto_bulk);
+  // stochastic rounding of 16-bit state: the head-run kernels' SR instances,
+  // whatever `algorithm` (the other kernels carry no generator)
+  const bool sr = sizeof(ST) == 2 && p.sr_seed != nullptr && !p.disable;
+  const bool bulk = !sr && (algorithm == 2 /* SSU_ALGO_BULK */ || (algorithm == 0 && auto_bulk));
   if (bulk) {
     const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
     const VarlenArgs v0 = va ? *va : VarlenArgs{};
@@ -188,14 +191,24 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
   const int64_t gz = (nitems + 65534) / 65535;
   const int64_t gy = (nitems + gz - 1) / gz;
   if (gx > 0x7fffffffLL || gz > 65535) return cudaErrorInvalidConfiguration;
-  const dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)gz);
+  dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)gz);
+  // calls that write no state: the no-write kernel on its (tiles, runs,
+  // sequences) grid up to 65535 sequences, beyond that the write kernel
+  // (which skips its stores) on the flattened grid -- one launch either way
+  const bool nowrite = p.disable && nitems <= 65535;
+  if (nowrite) grid = dim3((unsigned)p.tiles, (unsigned)(p.H / kh), (unsigned)nitems);
   const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
   const VarlenArgs v0 = va ? *va : VarlenArgs{};
-  auto kern = p.disable
+  auto kern = nowrite
                   ? (varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
                             : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>)
                   : (varlen ? ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
                             : ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>);
+  if constexpr (sizeof(ST) == 2) {
+    if (sr)
+      kern = varlen ? ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true, true>
+                    : ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false, true>;
+  }
   // several CTAs of up to 45 KB static shared memory per SM: ask for the
   // largest shared-memory carveout
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -223,6 +236,9 @@ cudaError_t launch_replay_typed(KParams p, const ReplayArgs& ra, int64_t nseqs,
   const int64_t gy = (nseqs + gz - 1) / gz;
   if (gx > 0x7fffffffLL || gz > 65535) return cudaErrorInvalidConfiguration;
   auto kern = ssu_replay_kernel<ST, IT, N, NT::WARPS, NT::UNR, kReplayLmax>;
+  if constexpr (sizeof(ST) == 2) {
+    if (p.sr_seed) kern = ssu_replay_kernel<ST, IT, N, NT::WARPS, NT::UNR, kReplayLmax, true>;
+  }
   const int smem = (int)sizeof(typename RC::Smem);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

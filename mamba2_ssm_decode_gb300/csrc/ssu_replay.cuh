@@ -271,7 +271,7 @@ struct ReplayCfg {
   using Smem = ReplaySmem<N, ROWS, LMAX, TILE_BYTES, WARPS>;
 };
 
-template <class ST, class IT, int N, int WARPS, int UNR, int LMAX>
+template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, bool SR = false>
 __global__ void __launch_bounds__(WARPS * 32, sizeof(ST) == 2 ? 3 : 16 / WARPS)
     ssu_replay_kernel(const KParams p, const ReplayArgs ra, int64_t nseqs, int kh,
                       unsigned* err) {
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(WARPS * 32, sizeof(ST) == 2 ? 3 : 16 / WARPS)
               if (prow < p.P) {
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c)
-                  store_state<ST>(state, ckpt - state + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
+                  store_state<ST, SR>(state, ckpt - state + (int64_t)prow * N + (q + c * L::LPR) * L::VEC,
                                   &hs[u][c * L::VEC / 2], p);
               }
             }
