@@ -247,34 +247,42 @@ __global__ void __launch_bounds__(256) ssd_chunk_state_kernel(const SSDArgs a) {
   };
   const int J = (Lc + kStSL - 1) / kStSL;
   uint32_t ph = 0;
+  static_assert(2 * kStSL * (P / 8) == 4 * NT, "four 16-byte pieces of w x per thread");
   for (int j = 0; j < J; ++j) {
+    // this thread's x pieces of the slice (8 p of one token each), fetched
+    // before waiting for the previous MMAs so the loads overlap them
+    uint4 raw[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int q = tid + r * NT;
+      const int k = q / (kStSL * (P / 8)), rem = q % (kStSL * (P / 8));
+      const int sl = rem % kStSL, pg = rem / kStSL, s = j * kStSL + sl;
+      raw[r] = (k < nh && s < Lc)
+                   ? __ldg(reinterpret_cast<const uint4*>(xg + ((t0 + s) * a.H + h0 + k) * P + pg * 8))
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
     if (j > 0) {  // the previous MMAs are done: the A buffer and B buffer (j + 1) % 2 are free
       wait(ph);
       ph ^= 1;
     }
     if (j + 1 < J) load_b(j + 1);
     tc::cp_commit();
-    // w x of the slice, 8 p of one token per 16-byte piece, split
-#pragma unroll 1
-    for (int q = tid; q < 2 * kStSL * (P / 8); q += NT) {
+    // w x of the slice, split into high parts and remainders
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int q = tid + r * NT;
       const int k = q / (kStSL * (P / 8)), rem = q % (kStSL * (P / 8));
       const int sl = rem % kStSL, pg = rem / kStSL, s = j * kStSL + sl;
-      uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = make_uint4(0u, 0u, 0u, 0u);
-      if (k < nh && s < Lc) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(xg + ((t0 + s) * a.H + h0 + k) * P + pg * 8));
-        const IT* e = reinterpret_cast<const IT*>(&raw);
-        const float ws = sm.w[k][s];
-        uint32_t hp[4], lp[4];
+      const IT* e = reinterpret_cast<const IT*>(&raw[r]);
+      const float ws = (k < nh && s < Lc) ? sm.w[k][s] : 0.0f;
+      uint32_t hp[4], lp[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          split_packed<IT>(ws * io_to_float<IT>(e[2 * u]), ws * io_to_float<IT>(e[2 * u + 1]), &hp[u],
-                           &lp[u]);
-        hi = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-        lo = make_uint4(lp[0], lp[1], lp[2], lp[3]);
-      }
+      for (int u = 0; u < 4; ++u)
+        split_packed<IT>(ws * io_to_float<IT>(e[2 * u]), ws * io_to_float<IT>(e[2 * u + 1]), &hp[u],
+                         &lp[u]);
       const int off = (k * 8 + pg) * 1024 + sl * 16;
-      *reinterpret_cast<uint4*>(sm.as[0] + off) = hi;
-      *reinterpret_cast<uint4*>(sm.as[1] + off) = lo;
+      *reinterpret_cast<uint4*>(sm.as[0] + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+      *reinterpret_cast<uint4*>(sm.as[1] + off) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
     }
     tc::cp_wait<1>();  // all but the newest group: B_j has landed
     tc::fence_proxy_async();
@@ -622,22 +630,31 @@ __global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
   const IT* zg = static_cast<const IT*>(a.z);
   const int64_t row = trow ? ((t0 + t) * a.H + h) * P : 0;
   uint32_t ph_cb = 0, ph_in = 0;
+  // this thread's row of CB for the slice in hand; the next slice's row is
+  // read while this one is processed (one tensor-memory round trip per slice
+  // hidden), except across the two halves of the chunk
+  float cb[16], cbn[16];
   for (int j = 0; j < J; ++j) {
     const int s0 = j * kSL;
-    if ((s0 % kHalf) == 0) {  // a new C . B^T block: wait for it
+    if ((s0 % kHalf) == 0) {  // a new C . B^T block: wait for it, read the slice
       wait(&sm.bar_cb, ph_cb);
       ph_cb ^= 1;
       tc::fence_after_sync();
+      tc::ld16(lane_base + kColCB + (s0 % kHalf) + 16 * wg, cb);
     }
+    tc::wait_ld();
+    if (j > 0 && (s0 % kHalf) != 0) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) cb[k] = cbn[k];
+    }
+    if (j + 1 < J && ((s0 + kSL) % kHalf) != 0)
+      tc::ld16(lane_base + kColCB + ((s0 + kSL) % kHalf) + 16 * wg, cbn);
     if (j == J - 1 && trow && wg == 0) {  // this row's x and z (one 128-byte line each) into L1
       asm volatile("prefetch.global.L1 [%0];" ::"l"(xg + row));
       if (zg) asm volatile("prefetch.global.L1 [%0];" ::"l"(zg + row));
     }
     // M_j, row t, columns [16 wg, 16 wg + 16) of the slice, into buffer j % 2
     // (free: M_{j-2} x_{j-2} is done)
-    float cb[16];
-    tc::ld16(lane_base + kColCB + (s0 % kHalf) + 16 * wg, cb);
-    tc::wait_ld();
     const int sb = s0 + 16 * wg;  // first source token of this thread's columns
     // With a_t non-increasing, exp(a_t - a_s) = exp(a_t - a_ref) exp(a_ref - a_s):
     // a slice wholly at or before t takes a_ref = its last token (both factors
