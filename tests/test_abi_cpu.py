@@ -232,6 +232,11 @@ def test_ssd_rejections(lib):
     assert call(params(nchunks=0)) == _abi.SSU_ERR_INVALID_ARGUMENT
     assert call(params(dt_min=1.0, dt_max=0.5)) == _abi.SSU_ERR_INVALID_ARGUMENT
     assert call(params(x=FAKE + 8)) == _abi.SSU_ERR_INVALID_ARGUMENT
+    assert call(params(states=FAKE + 8)) == _abi.SSU_ERR_INVALID_ARGUMENT   # vector stores
+    assert call(params(initial_states=FAKE + 4, initial_dtype=_abi.SSU_F32)) == \
+        _abi.SSU_ERR_INVALID_ARGUMENT
+    assert call(params(nheads=65536 * 2, ngroups=2)) == _abi.SSU_ERR_UNSUPPORTED  # grid y
+    assert call(params(nchunks=1 << 30)) == _abi.SSU_ERR_UNSUPPORTED
     assert call(params(), n=need - 1) == _abi.SSU_ERR_INVALID_ARGUMENT
     assert "workspace" in lib.ssu_last_error().decode()
 

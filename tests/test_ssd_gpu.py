@@ -197,3 +197,20 @@ def test_ssd_call_is_three_launches():
                                     D=c.D, z=c.z, dt_bias=c.dt_bias, dt_softplus=True,
                                     initial_states=c.initial_states, states=states, workspace=ws)
     assert graph_kernel_nodes(call) == 3
+
+
+def test_ssd_empty_chunks_and_chunks_shorter_than_a_tile(ssd_oracle):
+    """Chunks of no tokens (a sequence's state passes through unchanged and is
+    still reported for the chunk) and chunk boundaries that cut sequences into
+    pieces of 1..200 tokens, as the chunk metadata allows."""
+    c = W.ssd_case(lengths=[150, 90, 3], heads=8, headdim=64, dstate=128, groups=2,
+                   chunk_size=256, seed=17, device=DEV)
+    # sequence 0: [0, 40) [40, 40) [40, 150); sequence 1: [150, 151) [151, 240);
+    # sequence 2: [240, 240) [240, 243)
+    dev = c.cu_chunk_seqlens.device
+    c.cu_chunk_seqlens = torch.tensor([0, 40, 40, 150, 151, 240, 240, 243], dtype=torch.int64,
+                                      device=dev)
+    c.seq_idx = torch.tensor([0, 0, 0, 1, 1, 2, 2], dtype=torch.int64, device=dev)
+    c.last_chunk_indices = torch.tensor([2, 4, 6], dtype=torch.int64, device=dev)
+    parity(ssd_oracle, c, "empty chunks")
+    parity(ssd_oracle, c, "empty chunks, every chunk's state", return_intermediate_states=True)
