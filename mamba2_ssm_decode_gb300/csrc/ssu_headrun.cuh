@@ -1,8 +1,9 @@
 // ssu_headrun.cuh -- head-run kernels: one CTA takes a run of heads of one
 // group for one sequence (and one row tile), so the slot lookup, the B / C
 // staging and the per-head dt' / dA are done once for the run, and the state
-// tiles of the next heads (contiguous in the slot) land in shared memory by
-// cp.async while the current head computes.  Two kernels: calls that write
+// tiles of the next heads (contiguous in the slot) land in shared memory --
+// one bulk asynchronous copy per tile in the write kernel, 16-byte cp.async in
+// the no-write kernel -- while the current head computes.  Two kernels: calls that write
 // state (ssu_run_kernel, the step-by-step update of step_rows per head), and
 // calls that write no state (ssu_nowrite_kernel).
 //
@@ -753,8 +754,9 @@ struct StageView {
 // (sequence, run of kh heads of one group, row tile), placed by
 // head_run_coords.  The slot lookups, the chain's write
 // slots, B / C and the per-head dt' / dA table are formed once for the run;
-// each head's state tile lands in shared memory by cp.async, issued one head
-// ahead so it is in flight while the previous head computes; each head then
+// each head's state tile (its contiguous rows) lands in shared memory by one
+// bulk asynchronous copy on an mbarrier, issued one head ahead so it is in
+// flight while the previous head computes; each head then
 // runs step_rows on the same staged values, with the same stores, as the bulk
 // kernels (so the same bits).  Chains longer than LMAX take the per-head block
 // (ssu_block_on), head by head.
@@ -763,7 +765,7 @@ struct StageView {
 template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, bool VARLEN, bool SR = false>
 __global__ void __launch_bounds__(WARPS * 32, sizeof(ST) == 2 ? 3 : 16 / WARPS)
     ssu_run_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t nseqs,
-                   int kh) {
+                   int kh, unsigned* err) {
   using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
   using L = typename Cfg::L;
   constexpr int ROWS = Cfg::ROWS;
@@ -823,26 +825,26 @@ __global__ void __launch_bounds__(WARPS * 32, sizeof(ST) == 2 ? 3 : 16 / WARPS)
     dsts[i] = ok ? v : -1;
   }
 
-  // 1. the first head's state tile by 16-byte async copies (each head's tile
-  //    is issued one head ahead)
+  // 1. the first head's state tile by one bulk asynchronous copy (TMA
+  //    engine) on an mbarrier; each head's tile is issued one head ahead
   const int64_t block_elems = (int64_t)p.P * N;
   const int nrows = p.P - p0 < ROWS ? p.P - p0 : ROWS;
-  const int valid = read_ok ? nrows * N * (int)sizeof(ST) / 16 : 0;
+  const uint32_t tile_bytes = (uint32_t)(nrows * N * (int)sizeof(ST));
   const char* slot_rows = reinterpret_cast<const char*>(
       static_cast<const ST*>(p.state) + (read_ok ? src : 0) * p.H * block_elems +
       (int64_t)p0 * N);
+  __shared__ __align__(8) uint64_t tile_bar[2];
+  if (threadIdx.x == 0) {
+    mbar_init(&tile_bar[0], 1);
+    mbar_init(&tile_bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   auto issue_tile = [&](int k, int buf) {
-    if (k < kh) {
-      const char* gsrc = slot_rows + (size_t)(h0 + k) * block_elems * sizeof(ST);
-      unsigned char* dst = raw + buf * TILE_BYTES;
-#pragma unroll 4
-      for (int i = threadIdx.x; i < TILE_BYTES / 16; i += THREADS) {
-        const bool v = i < valid;
-        cp_async16(dst + i * 16, v ? gsrc + (size_t)i * 16 : static_cast<const char*>(p.state),
-                   v ? 16 : 0);
-      }
+    if (threadIdx.x == 0 && k < kh && read_ok) {
+      mbar_arrive_expect_tx(&tile_bar[buf], tile_bytes);
+      bulk_load(raw + buf * TILE_BYTES, slot_rows + (size_t)(h0 + k) * block_elems * sizeof(ST),
+                tile_bytes, &tile_bar[buf]);
     }
-    cp_async_commit();
   };
   issue_tile(0, 0);
 
@@ -862,11 +864,19 @@ __global__ void __launch_bounds__(WARPS * 32, sizeof(ST) == 2 ? 3 : 16 / WARPS)
   const int rr = lane / L::LPR;
   const int jbase = warp * UNR * L::RPW + rr;
   ST* state = static_cast<ST*>(p.state);
+  // a wait that runs out sets the error word; thread 0 then issues no more
+  // copies and, before the CTA ends, waits once more (bounded) for the one
+  // that did not land
+  bool dead = false;
+  int pend = -1;
   for (int k = 0; k < kh; ++k) {
-    cp_async_wait<0>();  // head k's copies
-    __syncthreads();     // ... from every thread; hrows[k & 1] complete; buffer
-                         // (k + 1) & 1 was read (head k - 1) before this point
-    issue_tile(k + 1, (k + 1) & 1);  // in flight during head k's steps
+    if (read_ok && !dead && !mbar_wait(&tile_bar[k & 1], (k >> 1) & 1)) {  // head k's tile
+      dead = true;
+      pend = k;
+      if (threadIdx.x == 0) atomicOr(err, kErrFullTimeout);
+    }
+    __syncthreads();  // hrows[k & 1] complete; buffer (k + 1) & 1 was read (head k - 1)
+    if (!dead) issue_tile(k + 1, (k + 1) & 1);  // in flight during head k's steps
     const int h = h0 + k;
     // 3. this thread's state chunks of head k, widened to fp32
     float2 hs[UNR][L::EPL / 2];
@@ -876,10 +886,13 @@ __global__ void __launch_bounds__(WARPS * 32, sizeof(ST) == 2 ? 3 : 16 / WARPS)
       for (int u = 0; u < UNR; ++u) {
         const int j = jbase + u * L::RPW;
 #pragma unroll
-        for (int c = 0; c < L::CPL; ++c)
-          Elem<ST>::unpack2(*reinterpret_cast<const uint4*>(
-                                tile + ((size_t)j * N + (q + c * L::LPR) * L::VEC) * sizeof(ST)),
-                            &hs[u][c * L::VEC / 2]);
+        for (int c = 0; c < L::CPL; ++c) {
+          const uint4 v = read_ok && j < nrows
+                              ? *reinterpret_cast<const uint4*>(
+                                    tile + ((size_t)j * N + (q + c * L::LPR) * L::VEC) * sizeof(ST))
+                              : make_uint4(0u, 0u, 0u, 0u);
+          Elem<ST>::unpack2(v, &hs[u][c * L::VEC / 2]);
+        }
       }
     }
     // 4. the next head's rows (into the other buffer)
@@ -911,6 +924,7 @@ __global__ void __launch_bounds__(WARPS * 32, sizeof(ST) == 2 ? 3 : 16 / WARPS)
       }
     }
   }
+  if (threadIdx.x == 0 && pend >= 0) mbar_wait(&tile_bar[pend & 1], (pend >> 1) & 1);
 }
 
 }  // namespace ssu

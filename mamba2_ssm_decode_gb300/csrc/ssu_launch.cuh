@@ -199,22 +199,33 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
   if (nowrite) grid = dim3((unsigned)p.tiles, (unsigned)(p.H / kh), (unsigned)nitems);
   const OneTokenArgs o0 = oa ? *oa : OneTokenArgs{};
   const VarlenArgs v0 = va ? *va : VarlenArgs{};
-  auto kern = nowrite
-                  ? (varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
-                            : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>)
-                  : (varlen ? ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
-                            : ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>);
+  auto kern2 = varlen ? ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
+                      : ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
   if constexpr (sizeof(ST) == 2) {
     if (sr)
-      kern = varlen ? ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true, true>
-                    : ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false, true>;
+      kern2 = varlen ? ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true, true>
+                     : ssu_run_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false, true>;
   }
-  // several CTAs of up to 45 KB static shared memory per SM: ask for the
-  // largest shared-memory carveout
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       (int)cudaSharedmemCarveoutMaxShared);
+  cudaError_t e;
+  if (nowrite) {
+    auto nk = varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
+                     : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
+    e = cudaFuncSetAttribute(nk, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  } else {
+    e = cudaFuncSetAttribute(kern2, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  }
   if (e != cudaSuccess) return e;
-  kern<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, nitems, kh);
+  unsigned* err = device_error_word();
+  if (!err) return cudaErrorInvalidSymbol;
+  if (nowrite) {
+    auto nk = varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
+                     : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
+    nk<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, nitems, kh);
+    return cudaGetLastError();
+  }
+  kern2<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, nitems, kh, err);
   return cudaGetLastError();
 }
 
