@@ -126,17 +126,21 @@ __device__ __forceinline__ bool spin_wait(uint64_t* bar, uint32_t parity, uint64
 //    is one M = 128 (two heads x 64 p) x N (dstate) MMA chain over the
 //    chunk's tokens, 64 at a time (K = tokens).  Both operands are MN-major,
 //    so x and B rows keep their global layout: 16-byte pieces (8 p, or 8 n,
-//    of one token) sit at (p / 8 or n / 8) 1024 + 16 s (LBO 128, SBO 1024).
+//    of one token) sit at (p / 8 or n / 8) 1040 + 16 s (LBO 128, SBO 1040: the
+//    16 bytes of padding per 64 tokens spread the eight pieces of one token's
+//    row over distinct banks, so the threads can take a token row's pieces
+//    side by side -- whole 128-byte lines from global memory).
 //    The A operand w x is computed, so it is split into high parts and
 //    remainders (two MMAs per step); B rows are copied in by cp.async one
 //    slice ahead.
 // ---------------------------------------------------------------------------
-constexpr int kStSL = 64;  // tokens per slice
+constexpr int kStSL = 64;     // tokens per slice
+constexpr int kStSBO = 1040;  // bytes between 8-row groups of the MN-major operands
 
 template <int N>
 struct StateSmem {
-  uint8_t as[2][128 * kStSL * 2];  // w x of the slice: high parts, remainders
-  uint8_t bs[2][N * kStSL * 2];    // B rows of a slice, two buffers
+  uint8_t as[2][16 * kStSBO];     // w x of the slice: high parts, remainders
+  uint8_t bs[2][N / 8 * kStSBO];  // B rows of a slice, two buffers
   float w[2][kMaxChunk];           // per head: a_t, then w_t
   uint64_t bar;
   uint32_t tmem;
@@ -173,10 +177,10 @@ __global__ void __launch_bounds__(256) ssd_chunk_state_kernel(const SSDArgs a) {
   auto load_b = [&](int j) {
 #pragma unroll 1
     for (int q = tid; q < kStSL * (N / 8); q += NT) {
-      const int sl = q % kStSL, ng = q / kStSL, s = j * kStSL + sl;
+      const int ng = q % (N / 8), sl = q / (N / 8), s = j * kStSL + sl;
       const bool ok = s < Lc;
-      tc::cp16(s_bs[j & 1] + ng * 1024 + sl * 16, bg + ((t0 + (ok ? s : 0)) * a.G + g) * N + ng * 8,
-               ok ? 16u : 0u);
+      tc::cp16(s_bs[j & 1] + ng * kStSBO + sl * 16,
+               bg + ((t0 + (ok ? s : 0)) * a.G + g) * N + ng * 8, ok ? 16u : 0u);
     }
   };
   load_b(0);
@@ -255,8 +259,8 @@ __global__ void __launch_bounds__(256) ssd_chunk_state_kernel(const SSDArgs a) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int q = tid + r * NT;
-      const int k = q / (kStSL * (P / 8)), rem = q % (kStSL * (P / 8));
-      const int sl = rem % kStSL, pg = rem / kStSL, s = j * kStSL + sl;
+      const int pg = q % (P / 8), rest = q / (P / 8);
+      const int sl = rest % kStSL, k = rest / kStSL, s = j * kStSL + sl;
       raw[r] = (k < nh && s < Lc)
                    ? __ldg(reinterpret_cast<const uint4*>(xg + ((t0 + s) * a.H + h0 + k) * P + pg * 8))
                    : make_uint4(0u, 0u, 0u, 0u);
@@ -271,8 +275,8 @@ __global__ void __launch_bounds__(256) ssd_chunk_state_kernel(const SSDArgs a) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int q = tid + r * NT;
-      const int k = q / (kStSL * (P / 8)), rem = q % (kStSL * (P / 8));
-      const int sl = rem % kStSL, pg = rem / kStSL, s = j * kStSL + sl;
+      const int pg = q % (P / 8), rest = q / (P / 8);
+      const int sl = rest % kStSL, k = rest / kStSL, s = j * kStSL + sl;
       const IT* e = reinterpret_cast<const IT*>(&raw[r]);
       const float ws = (k < nh && s < Lc) ? sm.w[k][s] : 0.0f;
       uint32_t hp[4], lp[4];
@@ -280,7 +284,7 @@ __global__ void __launch_bounds__(256) ssd_chunk_state_kernel(const SSDArgs a) {
       for (int u = 0; u < 4; ++u)
         split_packed<IT>(ws * io_to_float<IT>(e[2 * u]), ws * io_to_float<IT>(e[2 * u + 1]), &hp[u],
                          &lp[u]);
-      const int off = (k * 8 + pg) * 1024 + sl * 16;
+      const int off = (k * 8 + pg) * kStSBO + sl * 16;
       *reinterpret_cast<uint4*>(sm.as[0] + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
       *reinterpret_cast<uint4*>(sm.as[1] + off) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
     }
@@ -294,8 +298,8 @@ __global__ void __launch_bounds__(256) ssd_chunk_state_kernel(const SSDArgs a) {
       for (int part = 0; part < 2; ++part)
 #pragma unroll
         for (int kk = 0; kk < kStSL / 16; ++kk)
-          tc::mma(tmem, tc::sdesc(s_as[part] + kk * 256, 128, 1024),
-                  tc::sdesc(s_bs[j & 1] + kk * 256, 128, 1024), kId, (j | part | kk) != 0);
+          tc::mma(tmem, tc::sdesc(s_as[part] + kk * 256, 128, kStSBO),
+                  tc::sdesc(s_bs[j & 1] + kk * 256, 128, kStSBO), kId, (j | part | kk) != 0);
       tc::commit(smem_addr(&sm.bar));
     }
   }
@@ -482,7 +486,9 @@ __global__ void __launch_bounds__(128) ssd_state_passing_kernel(const SSDArgs a)
 //      bs  B rows of one half (128 source tokens), K-major: (s, n / 8) at
 //          (n / 8) 2048 + 16 s                       (LBO 2048, SBO 128)
 //      xs  x rows of a slice (two buffers), MN-major [64 p x 32 s]: the 8 p
-//          of (p / 8, s) at (p / 8) 512 + 16 s       (LBO 128, SBO 512)
+//          of (p / 8, s) at (p / 8) 528 + 16 s       (LBO 128, SBO 528; the
+//          padding spreads one token's 8 pieces over distinct banks, so
+//          neighbouring threads copy one token's 128-byte row)
 // ---------------------------------------------------------------------------
 constexpr int kTB = 128;               // query rows per CTA (the MMA M)
 constexpr int kSL = 32;                // source tokens per slice
@@ -491,13 +497,14 @@ constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColInter = 0, kColIntra = 64, kColCB = 128;
 constexpr int kScanMinSmem = 78 * 1024;  // at most two CTAs per SM: 2 x 256 columns
 constexpr int kMBytes = kTB * kSL * 2;   // one part (high or remainder) of M_j
+constexpr int kXsSBO = 528;              // bytes between 8-p groups of an x slice
 
 template <int P, int N>
 struct ScanSmem {
   uint8_t cq[kTB * N * 2];
   uint8_t hm[(2 * P * N * 2 > 4 * kMBytes) ? 2 * P * N * 2 : 4 * kMBytes];
   uint8_t bs[kHalf * N * 2];
-  uint8_t xs[2][kSL * P * 2];
+  uint8_t xs[2][P / 8 * kXsSBO];
   float acum[kMaxChunk], dtp[kMaxChunk], q[kMaxChunk], qs[kMaxChunk];
   int tame[kMaxChunk / kSL];
   uint64_t bar_h, bar_cb, bar_intra;
@@ -550,11 +557,11 @@ __global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
                ok ? 16u : 0u);
     }
   };
-  auto load_x = [&](int j) {  // one 16-byte piece per thread
-    const int sl = tid % kSL, pg = tid / kSL, s = j * kSL + sl;
+  auto load_x = [&](int j) {  // one 16-byte piece per thread, a token's 8 side by side
+    const int pg = tid % (P / 8), sl = tid / (P / 8), s = j * kSL + sl;
     const bool ok = s < Lc;
-    tc::cp16(s_xs[j & 1] + pg * 512 + sl * 16, xg + ((t0 + (ok ? s : 0)) * a.H + h) * P + pg * 8,
-             ok ? 16u : 0u);
+    tc::cp16(s_xs[j & 1] + pg * kXsSBO + sl * 16,
+             xg + ((t0 + (ok ? s : 0)) * a.H + h) * P + pg * 8, ok ? 16u : 0u);
   };
   static_assert(kSL * (P / 8) == NT, "one x piece per thread");
   load_rows(s_cq, cg, r0);
@@ -727,7 +734,7 @@ __global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
 #pragma unroll
         for (int kk = 0; kk < kSL / 16; ++kk)
           tc::mma(tmem + kColIntra, tc::sdesc(s_m + part * kMBytes + kk * 256, 128, 512),
-                  tc::sdesc(s_xs[j & 1] + kk * 256, 128, 512), kIdIntra, (j | part | kk) != 0);
+                  tc::sdesc(s_xs[j & 1] + kk * 256, 128, kXsSBO), kIdIntra, (j | part | kk) != 0);
       tc::commit(smem_addr(&sm.bar_intra));
     }
   }
