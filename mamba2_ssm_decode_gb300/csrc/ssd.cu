@@ -461,18 +461,19 @@ __global__ void __launch_bounds__(128) ssd_state_passing_kernel(const SSDArgs a)
 
 // ---------------------------------------------------------------------------
 // 3. the scan on the fifth-generation tensor cores: y of up to 128 query
-//    tokens (one t-block) of one chunk and head per CTA of 256 threads (two
+//    tokens (one t-block) of one chunk and head per CTA of 512 threads (four
 //    warpgroups).  Thread i of each warpgroup owns query row t = 128 tb + i,
 //    which is also tensor-memory lane i of every M = 128 accumulator:
 //      columns [0, 64)    C_t . h_enter             (K = N, h_enter split)
 //      columns [64, 128)  sum_s M[t,s] x_s          (K = 32 source tokens per slice)
 //      columns [128, 256) CB = C . B^T for 128 source tokens (one half of the chunk)
 //    The tensor core forms CB for source tokens [0, 128) up front and, for the
-//    second t-block, CB for [128, 256) once the first half has been read.
+//    second t-block, CB for [128, 256) once the first half has been read (its
+//    B rows are copied in during slices 0 to 2).
 //    Source slice j (tokens [32 j, 32 j + 32), up to the t-block's last row):
-//    each thread reads its row of CB, decays and masks it (M[t,s] = CB[t,s]
-//    exp(a_t - a_s) dt'_s for s <= t), splits it into high parts and
-//    remainders in shared memory (two buffers), and the tensor core adds
+//    each thread reads 8 columns of its row of CB, decays and masks them
+//    (M[t,s] = CB[t,s] exp(a_t - a_s) dt'_s for s <= t), splits them into high
+//    parts and remainders in shared memory (two buffers), and the tensor core adds
 //    M_j x_j while the threads go on to slice j + 1; x rows are copied
 //    (cp.async) one slice ahead.
 //    Shared-memory operands (no-swizzle canonical layouts, see ssd_tc.cuh):
@@ -512,17 +513,17 @@ struct ScanSmem {
 };
 
 template <class IT, int P, int N>
-__global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
+__global__ void __launch_bounds__(512, 2) ssd_chunk_scan_kernel(const SSDArgs a) {
   static_assert(P == 64 && (N == 64 || N == 128), "headdim 64, dstate 64 or 128");
   constexpr bool kBF16 = std::is_same<IT, __nv_bfloat16>::value;
   constexpr uint32_t kIdInter = tc::idesc_f16(kBF16, kTB, 64, false, false);
   constexpr uint32_t kIdCB = tc::idesc_f16(kBF16, kTB, kHalf, false, false);
   constexpr uint32_t kIdIntra = tc::idesc_f16(kBF16, kTB, 64, false, true);
-  constexpr int NT = 256;
+  constexpr int NT = 512;
   const int c = blockIdx.x >> 1, tb = blockIdx.x & 1, h = blockIdx.y;
-  // two warpgroups: both cover the 128 rows (tensor-memory lanes); warpgroup
-  // wg takes columns [16 wg, 16 wg + 16) of each source slice and output
-  // columns [32 wg, 32 wg + 32)
+  // four warpgroups: each covers the 128 rows (tensor-memory lanes); warpgroup
+  // wg takes columns [8 wg, 8 wg + 8) of each source slice and output
+  // columns [16 wg, 16 wg + 16)
   const int tid = threadIdx.x, warp = tid >> 5, wg = warp >> 2, lrow = tid & 127;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   auto& sm = *reinterpret_cast<ScanSmem<P, N>*>(smem_raw);
@@ -563,10 +564,10 @@ __global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
     tc::cp16(s_xs[j & 1] + pg * kXsSBO + sl * 16,
              xg + ((t0 + (ok ? s : 0)) * a.H + h) * P + pg * 8, ok ? 16u : 0u);
   };
-  static_assert(kSL * (P / 8) == NT, "one x piece per thread");
+  static_assert(kSL * (P / 8) == NT / 2, "one x piece per thread of the first half");
   load_rows(s_cq, cg, r0);
   load_rows(s_bs, bg, 0);
-  load_x(0);
+  if (tid < NT / 2) load_x(0);
   tc::cp_commit();
   if (tid == 0) {
     mbar_init(&sm.bar_h, 1);
@@ -633,36 +634,37 @@ __global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
   const int tt = trow ? t : -1;  // no source token is at or before a row past the chunk
   const float at = trow ? sm.acum[t] : 0.0f;
   const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-  const int m_row = (lrow >> 3) * 512 + (lrow & 7) * 16 + wg * 256;  // + kg 128, kg in {2 wg, 2 wg + 1}
+  const int m_row = (lrow >> 3) * 512 + (lrow & 7) * 16 + wg * 128;  // 8-column group kg = wg
   const IT* zg = static_cast<const IT*>(a.z);
   const int64_t row = trow ? ((t0 + t) * a.H + h) * P : 0;
   uint32_t ph_cb = 0, ph_in = 0;
+  const bool two_halves = J * kSL > kHalf;
   // this thread's row of CB for the slice in hand; the next slice's row is
   // read while this one is processed (one tensor-memory round trip per slice
   // hidden), except across the two halves of the chunk
-  float cb[16], cbn[16];
+  float cb[8], cbn[8];
   for (int j = 0; j < J; ++j) {
     const int s0 = j * kSL;
     if ((s0 % kHalf) == 0) {  // a new C . B^T block: wait for it, read the slice
       wait(&sm.bar_cb, ph_cb);
       ph_cb ^= 1;
       tc::fence_after_sync();
-      tc::ld16(lane_base + kColCB + (s0 % kHalf) + 16 * wg, cb);
+      tc::ld8(lane_base + kColCB + (s0 % kHalf) + 8 * wg, cb);
     }
     tc::wait_ld();
     if (j > 0 && (s0 % kHalf) != 0) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) cb[k] = cbn[k];
+      for (int k = 0; k < 8; ++k) cb[k] = cbn[k];
     }
     if (j + 1 < J && ((s0 + kSL) % kHalf) != 0)
-      tc::ld16(lane_base + kColCB + ((s0 + kSL) % kHalf) + 16 * wg, cbn);
+      tc::ld8(lane_base + kColCB + ((s0 + kSL) % kHalf) + 8 * wg, cbn);
     if (j == J - 1 && trow && wg == 0) {  // this row's x and z (one 128-byte line each) into L1
       asm volatile("prefetch.global.L1 [%0];" ::"l"(xg + row));
       if (zg) asm volatile("prefetch.global.L1 [%0];" ::"l"(zg + row));
     }
-    // M_j, row t, columns [16 wg, 16 wg + 16) of the slice, into buffer j % 2
+    // M_j, row t, columns [8 wg, 8 wg + 8) of the slice, into buffer j % 2
     // (free: M_{j-2} x_{j-2} is done)
-    const int sb = s0 + 16 * wg;  // first source token of this thread's columns
+    const int sb = s0 + 8 * wg;  // first source token of this thread's columns
     // With a_t non-increasing, exp(a_t - a_s) = exp(a_t - a_ref) exp(a_ref - a_s):
     // a slice wholly at or before t takes a_ref = its last token (both factors
     // <= 1); the slice holding t takes a_ref = its first token when the slice
@@ -682,51 +684,47 @@ __global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
       }
     }
     uint8_t* m_hi = sm.hm + (j & 1) * (2 * kMBytes) + m_row;
-#pragma unroll
-    for (int kh = 0; kh < 2; ++kh) {
+    {
       uint32_t hp[4], lp[4];
 #pragma unroll
       for (int k = 0; k < 8; k += 2) {
         float v[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int s = sb + kh * 8 + k + e;
+          const int s = sb + k + e;
           float f;
           if (!per_entry) f = s <= tt ? rf * tab[s] : 0.0f;
           else f = s <= tt ? __expf(at - sm.acum[s]) * sm.dtp[s] : 0.0f;
-          v[e] = cb[kh * 8 + k + e] * f;
+          v[e] = cb[k + e] * f;
         }
         split_packed<IT>(v[0], v[1], &hp[k / 2], &lp[k / 2]);
       }
-      *reinterpret_cast<uint4*>(m_hi + kh * 128) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-      *reinterpret_cast<uint4*>(m_hi + kMBytes + kh * 128) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
-    }
-    if (s0 + kSL == kHalf && J * kSL > kHalf) {
-      // every row of the first half's CB is read: B rows [128, 256) into bs
-      // (CB of the first half is done with it), then C . B^T of the second half
-      tc::fence_before_sync();
-      __syncthreads();
-      load_rows(s_bs, bg, kHalf);
-      tc::cp_commit();
-      tc::cp_wait<0>();
-      tc::fence_proxy_async();
-      tc::fence_before_sync();
-      __syncthreads();
-      tc::fence_after_sync();
-      if (tid == 0) issue_cb();
+      *reinterpret_cast<uint4*>(m_hi) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+      *reinterpret_cast<uint4*>(m_hi + kMBytes) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
     }
     if (j > 0) {  // M_{j-1} x_{j-1} done: x buffer (j + 1) % 2 and M buffer (j + 1) % 2 free
       wait(&sm.bar_intra, ph_in);
       ph_in ^= 1;
     }
-    if (j + 1 < J) load_x(j + 1);
+    if (j + 1 < J && tid < NT / 2) load_x(j + 1);
     tc::cp_commit();
-    tc::cp_wait<1>();  // all but x_{j+1}: x_j has landed
+    if (two_halves && j == 0) {
+      // the first half's C . B^T has read bs (its barrier was waited for
+      // above): B rows [128, 256) go in now, one group behind x_1, and must
+      // have landed by slice 2 (the copy groups complete in order)
+      load_rows(s_bs, bg, kHalf);
+      tc::cp_commit();
+    }
+    if (two_halves && j < 2) tc::cp_wait<2>();  // x_j has landed (B may still be in flight)
+    else tc::cp_wait<1>();                      // all but x_{j+1}: x_j (and B) have landed
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) {
+      // every row of the first half's CB has been read (each thread waited
+      // for its last read before the barrier): C . B^T of the second half
+      if (two_halves && s0 + kSL == kHalf) issue_cb();
       // sum_s M[t,s] x_s: high parts, then remainders
       const uint32_t s_m = s_hm + (j & 1) * (2 * kMBytes);
 #pragma unroll
@@ -741,34 +739,31 @@ __global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
   wait(&sm.bar_intra, ph_in);  // the last M x done: every accumulator is final
   tc::fence_after_sync();
   // y = intra + exp(a_t) C_t . h_enter + D x_t, times silu(z_t): output
-  // columns [32 wg, 32 wg + 32) of row t
+  // columns [16 wg, 16 wg + 16) of row t
   IT* og = static_cast<IT*>(a.out);
   const float dec = expf(at);
   const float Dh = (a.D && !a.D_per_dim) ? a.D[h] : 0.0f;
 #pragma unroll 1
-  for (int c16 = 2 * wg; c16 < 2 * wg + 2; ++c16) {
-    float yi[16], yo[16];
-    tc::ld16(lane_base + kColInter + c16 * 16, yi);
-    tc::ld16(lane_base + kColIntra + c16 * 16, yo);
-    uint4 xq[2], zq[2];
+  for (int c8 = 2 * wg; c8 < 2 * wg + 2; ++c8) {
+    float yi[8], yo[8];
+    tc::ld8(lane_base + kColInter + c8 * 8, yi);
+    tc::ld8(lane_base + kColIntra + c8 * 8, yo);
+    uint4 xq = make_uint4(0u, 0u, 0u, 0u), zq = make_uint4(0u, 0u, 0u, 0u);
     if (trow) {
-      xq[0] = __ldg(reinterpret_cast<const uint4*>(xg + row) + 2 * c16);
-      xq[1] = __ldg(reinterpret_cast<const uint4*>(xg + row) + 2 * c16 + 1);
-      zq[0] = zg ? __ldg(reinterpret_cast<const uint4*>(zg + row) + 2 * c16) : make_uint4(0u, 0u, 0u, 0u);
-      zq[1] = zg ? __ldg(reinterpret_cast<const uint4*>(zg + row) + 2 * c16 + 1)
-                 : make_uint4(0u, 0u, 0u, 0u);
+      xq = __ldg(reinterpret_cast<const uint4*>(xg + row) + c8);
+      if (zg) zq = __ldg(reinterpret_cast<const uint4*>(zg + row) + c8);
     }
     tc::wait_ld();
     if (trow) {
-      const IT* xv = reinterpret_cast<const IT*>(&xq[0]);
-      const IT* zv = reinterpret_cast<const IT*>(&zq[0]);
-      uint32_t packed[8];
+      const IT* xv = reinterpret_cast<const IT*>(&xq);
+      const IT* zv = reinterpret_cast<const IT*>(&zq);
+      uint32_t packed[4];
 #pragma unroll
-      for (int k = 0; k < 16; k += 2) {
+      for (int k = 0; k < 8; k += 2) {
         float v[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int p = c16 * 16 + k + e;
+          const int p = c8 * 8 + k + e;
           float y = yo[k + e] + dec * yi[k + e];
           const float x = io_to_float<IT>(xv[k + e]);
           if (a.D) y += (a.D_per_dim ? a.D[h * P + p] : Dh) * x;
@@ -780,10 +775,7 @@ __global__ void __launch_bounds__(256) ssd_chunk_scan_kernel(const SSDArgs a) {
         }
         packed[k / 2] = pack_pair<IT>(v[0], v[1]);
       }
-      reinterpret_cast<uint4*>(og + row)[2 * c16] =
-          make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      reinterpret_cast<uint4*>(og + row)[2 * c16 + 1] =
-          make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      reinterpret_cast<uint4*>(og + row)[c8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
   }
   tc::fence_before_sync();
@@ -811,7 +803,7 @@ cudaError_t launch(const SSDArgs& a, cudaStream_t stream) {
   if ((e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
       cudaSuccess)
     return e;
-  scan<<<dim3((unsigned)a.nchunks * 2, a.H), 256, smem, stream>>>(a);
+  scan<<<dim3((unsigned)a.nchunks * 2, a.H), 512, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -2,8 +2,9 @@
 // group for one sequence (and one row tile), so the slot lookup, the B / C
 // staging and the per-head dt' / dA are done once for the run, and the state
 // tiles of the next heads (contiguous in the slot) land in shared memory --
-// one bulk asynchronous copy per tile in the write kernel, 16-byte cp.async in
-// the no-write kernel -- while the current head computes.  Two kernels: calls that write
+// one bulk asynchronous copy per tile, or 16-byte cp.async where the no-write
+// kernel's tensor-core dot products want a swizzled tile -- while the current
+// head computes.  Two kernels: calls that write
 // state (ssu_run_kernel, the step-by-step update of step_rows per head), and
 // calls that write no state (ssu_nowrite_kernel).
 //
@@ -509,7 +510,7 @@ __device__ __forceinline__ bool head_run_coords(const KParams& p, int64_t nseqs,
 template <class ST, class IT, int N, int WARPS, int UNR, int LMAX, bool VARLEN>
 __global__ void __launch_bounds__(WARPS * 32, 5)
     ssu_nowrite_kernel(const KParams p, const OneTokenArgs oa, const VarlenArgs va, int64_t nseqs,
-                       int kh) {
+                       int kh, unsigned* err) {
   using Cfg = SSUConfig<ST, IT, N, WARPS, UNR, LMAX>;
   using L = typename Cfg::L;
   constexpr int ROWS = Cfg::ROWS;
@@ -554,15 +555,33 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
     return;
   }
 
-  // 1. state tiles of the first two heads by 16-byte async copies (zero fill
-  //    past P or without a read slot), one commit group per head
+  // 1. state tiles of the first two heads: with the tensor-core dot products
+  //    by 16-byte async copies into the swizzled layout (zero fill past P or
+  //    without a read slot), one commit group per head; otherwise each tile
+  //    (the head's contiguous rows) by one bulk asynchronous copy on an
+  //    mbarrier, and rows past P or without a read slot read as zeros
   const int64_t block_elems = (int64_t)p.P * N;
   const int nrows = p.P - p0 < ROWS ? p.P - p0 : ROWS;
   const int valid = read_ok ? nrows * N * (int)sizeof(ST) / 16 : 0;
   const char* slot_rows = reinterpret_cast<const char*>(
       static_cast<const ST*>(p.state) + (read_ok ? src : 0) * p.H * block_elems +
       (int64_t)p0 * N);
+  __shared__ __align__(8) uint64_t tile_bar[2];
+  if (!MMA && threadIdx.x == 0) {
+    mbar_init(&tile_bar[0], 1);
+    mbar_init(&tile_bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   auto issue_tile = [&](int k, int buf) {
+    if constexpr (!MMA) {
+      if (threadIdx.x == 0 && k < kh && read_ok) {
+        const uint32_t bytes = (uint32_t)(nrows * N * (int)sizeof(ST));
+        mbar_arrive_expect_tx(&tile_bar[buf], bytes);
+        bulk_load(raw + buf * TILE_BYTES, slot_rows + (size_t)(h0 + k) * block_elems * sizeof(ST),
+                  bytes, &tile_bar[buf]);
+      }
+      return;
+    }
     if (k < kh) {
       const char* gsrc = slot_rows + (size_t)(h0 + k) * block_elems * sizeof(ST);
       unsigned char* dst = raw + buf * TILE_BYTES;
@@ -618,9 +637,20 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
   const int q = lane % L::LPR;
   const int rr = lane / L::LPR;
   const int jbase = warp * UNR * L::RPW + rr;
+  // a wait that runs out sets the error word; thread 0 then issues no more
+  // copies and, before the CTA ends, waits once more (bounded) for the ones
+  // still in flight
+  bool dead = false;
+  int pend = -1;
   for (int k = 0; k < kh; ++k) {
-    cp_async_wait<1>();  // head k's copies (the newest group is head k + 1's)
-    __syncthreads();     // ... from every thread; hrows[k & 1] and G complete
+    if constexpr (MMA) {
+      cp_async_wait<1>();  // head k's copies (the newest group is head k + 1's)
+    } else if (read_ok && !dead && !mbar_wait(&tile_bar[k & 1], (k >> 1) & 1)) {
+      dead = true;
+      pend = k;
+      if (threadIdx.x == 0) atomicOr(err, kErrFullTimeout);
+    }
+    __syncthreads();  // head k's tile from every copy; hrows[k & 1] and G complete
     const unsigned char* tile = raw + (k & 1) * TILE_BYTES;
 
     // 3. ct[t] = C_t . h for this thread's rows: one pass over the tile
@@ -653,9 +683,12 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
       for (int u = 0; u < UNR; ++u) {
         const int j = jbase + u * L::RPW;
         float2 hv[C2];
-        Elem<ST>::unpack2(*reinterpret_cast<const uint4*>(
-                              tile + ((size_t)j * N + (q + c * L::LPR) * L::VEC) * sizeof(ST)),
-                          hv);
+        const uint4 hraw =
+            read_ok && j < nrows
+                ? *reinterpret_cast<const uint4*>(
+                      tile + ((size_t)j * N + (q + c * L::LPR) * L::VEC) * sizeof(ST))
+                : make_uint4(0u, 0u, 0u, 0u);
+        Elem<ST>::unpack2(hraw, hv);
 #pragma unroll
         for (int t = 0; t < LMAX; ++t) {
           if (t >= len) break;
@@ -701,7 +734,7 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
       pre.finish<true>(hrows[(k + 1) & 1], p, len, p0, tied, hsteps.dt[k + 1], hsteps.dA[k + 1]);
     if (k + 2 < kh) pre.load(p, h0 + k + 2, tied);
     __syncthreads();  // every thread is done with tile k; hrows[(k + 1) & 1] complete
-    issue_tile(k + 2, k & 1);
+    if (!dead) issue_tile(k + 2, k & 1);
 
     // 5. y of head k
     if constexpr (MMA) {
@@ -731,6 +764,13 @@ __global__ void __launch_bounds__(WARPS * 32, 5)
         if (p0 + j < p.P)
           closed_form_y<IT, LMAX>(p, hrows[k & 1], G, ct[i], len, j, h0 + k, p0 + j, r0);
       }
+    }
+  }
+  if constexpr (!MMA) {
+    // after a timeout: the copy that did not land and the one issued after it
+    if (threadIdx.x == 0 && pend >= 0) {
+      mbar_wait(&tile_bar[pend & 1], (pend >> 1) & 1);
+      if (pend + 1 < kh) mbar_wait(&tile_bar[(pend + 1) & 1], ((pend + 1) >> 1) & 1);
     }
   }
 }

@@ -222,7 +222,7 @@ cudaError_t launch_typed(bool varlen, KParams p, const OneTokenArgs* oa, const V
   if (nowrite) {
     auto nk = varlen ? ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, T::LMAX, true>
                      : ssu_nowrite_kernel<ST, IT, N, NT::WARPS, NT::UNR, 1, false>;
-    nk<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, nitems, kh);
+    nk<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, nitems, kh, err);
     return cudaGetLastError();
   }
   kern2<<<grid, NT::WARPS * 32, 0, stream>>>(p, o0, v0, nitems, kh, err);
