@@ -475,7 +475,8 @@ __global__ void __launch_bounds__(128) ssd_state_passing_kernel(const SSDArgs a)
 //    (M[t,s] = CB[t,s] exp(a_t - a_s) dt'_s for s <= t), splits them into high
 //    parts and remainders in shared memory (two buffers), and the tensor core adds
 //    M_j x_j while the threads go on to slice j + 1; x rows are copied
-//    (cp.async) one slice ahead.
+//    (cp.async) one slice ahead.  Once the last C . B^T is done, the x and z
+//    rows of the t-block are copied into the C and B tiles for the epilogue.
 //    Shared-memory operands (no-swizzle canonical layouts, see ssd_tc.cuh):
 //      cq  C rows of the t-block, K-major: core-matrix row (r, n / 8) at
 //          (n / 8) 2048 + 16 r                       (LBO 2048, SBO 128)
@@ -515,6 +516,7 @@ struct ScanSmem {
 template <class IT, int P, int N>
 __global__ void __launch_bounds__(512, 2) ssd_chunk_scan_kernel(const SSDArgs a) {
   static_assert(P == 64 && (N == 64 || N == 128), "headdim 64, dstate 64 or 128");
+  static_assert(kTB * P * 2 <= kTB * N * 2 && kTB * P * 2 <= kHalf * N * 2, "x / z rows fit the C / B tiles");
   constexpr bool kBF16 = std::is_same<IT, __nv_bfloat16>::value;
   constexpr uint32_t kIdInter = tc::idesc_f16(kBF16, kTB, 64, false, false);
   constexpr uint32_t kIdCB = tc::idesc_f16(kBF16, kTB, kHalf, false, false);
@@ -650,6 +652,23 @@ __global__ void __launch_bounds__(512, 2) ssd_chunk_scan_kernel(const SSDArgs a)
       ph_cb ^= 1;
       tc::fence_after_sync();
       tc::ld8(lane_base + kColCB + (s0 % kHalf) + 8 * wg, cb);
+      if (s0 + kHalf >= J * kSL) {
+        // the last MMA reading the C and B rows is done: the epilogue's x rows
+        // of the t-block go where the C rows were, its z rows where the B rows
+        // were (row r's 16-byte piece k at (k ^ r % 8), so the epilogue's reads
+        // of one piece of 32 rows spread over all banks); they join the next x
+        // slice's copy group
+#pragma unroll
+        for (int u = 0; u < (kTB * 8 * 2) / NT; ++u) {
+          const int q = tid + u * NT, which = q / (kTB * 8), r = (q / 8) % kTB, k = q % 8;
+          const IT* src = which ? zg : xg;
+          if (src) {
+            const bool ok = r0 + r < Lc;
+            tc::cp16((which ? s_bs : s_cq) + r * 128 + ((k ^ (r & 7)) << 4),
+                     src + ((t0 + (ok ? r0 + r : 0)) * a.H + h) * P + k * 8, ok ? 16u : 0u);
+          }
+        }
+      }
     }
     tc::wait_ld();
     if (j > 0 && (s0 % kHalf) != 0) {
@@ -658,10 +677,6 @@ __global__ void __launch_bounds__(512, 2) ssd_chunk_scan_kernel(const SSDArgs a)
     }
     if (j + 1 < J && ((s0 + kSL) % kHalf) != 0)
       tc::ld8(lane_base + kColCB + ((s0 + kSL) % kHalf) + 8 * wg, cbn);
-    if (j == J - 1 && trow && wg == 0) {  // this row's x and z (one 128-byte line each) into L1
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(xg + row));
-      if (zg) asm volatile("prefetch.global.L1 [%0];" ::"l"(zg + row));
-    }
     // M_j, row t, columns [8 wg, 8 wg + 8) of the slice, into buffer j % 2
     // (free: M_{j-2} x_{j-2} is done)
     const int sb = s0 + 8 * wg;  // first source token of this thread's columns
@@ -737,6 +752,9 @@ __global__ void __launch_bounds__(512, 2) ssd_chunk_scan_kernel(const SSDArgs a)
     }
   }
   wait(&sm.bar_intra, ph_in);  // the last M x done: every accumulator is final
+  tc::cp_wait<0>();             // this thread's pieces of the x and z rows
+  tc::fence_before_sync();
+  __syncthreads();              // ... and every other thread's
   tc::fence_after_sync();
   // y = intra + exp(a_t) C_t . h_enter + D x_t, times silu(z_t): output
   // columns [16 wg, 16 wg + 16) of row t
@@ -750,8 +768,9 @@ __global__ void __launch_bounds__(512, 2) ssd_chunk_scan_kernel(const SSDArgs a)
     tc::ld8(lane_base + kColIntra + c8 * 8, yo);
     uint4 xq = make_uint4(0u, 0u, 0u, 0u), zq = make_uint4(0u, 0u, 0u, 0u);
     if (trow) {
-      xq = __ldg(reinterpret_cast<const uint4*>(xg + row) + c8);
-      if (zg) zq = __ldg(reinterpret_cast<const uint4*>(zg + row) + c8);
+      const int off = lrow * 128 + ((c8 ^ (lrow & 7)) << 4);
+      xq = *reinterpret_cast<const uint4*>(sm.cq + off);
+      if (zg) zq = *reinterpret_cast<const uint4*>(sm.bs + off);
     }
     tc::wait_ld();
     if (trow) {
