@@ -439,11 +439,19 @@ def measured_peak():
 DATA = "synthetic (seeded random inputs of Mamba2 serving shapes)"
 
 
+def _code_only(src):
+    """C / CUDA source text without comments and with whitespace collapsed."""
+    text = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(workload=None):
     """Hash of the CUDA sources a workload's kernels are built from: the SSD
     prefill's (ssd* and the three SSU headers it includes) or the SSU decode's
     (every other source), so that a change to one leaves the other's ncu
-    traffic record valid."""
+    traffic record valid.  Only the code is hashed: an edit to comments or
+    whitespace leaves the records valid."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mamba2_ssm_decode_gb300", "csrc")
     ssd = workload == SSD_WORKLOAD
@@ -451,8 +459,8 @@ def kernel_source_hash(workload=None):
         if f.startswith("ssd") != ssd and not (ssd and f in ("ssu_headrun.cuh", "ssu_kernel.cuh",
                                                           "ssu_bulk.cuh")):
             continue
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8", errors="replace") as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -491,6 +491,9 @@ __global__ void __launch_bounds__(128) ssd_state_passing_kernel(const SSDArgs a)
 //          of (p / 8, s) at (p / 8) 528 + 16 s       (LBO 128, SBO 528; the
 //          padding spreads one token's 8 pieces over distinct banks, so
 //          neighbouring threads copy one token's 128-byte row)
+//    After the last C . B^T: cq holds the x rows and bs the z rows of the
+//    t-block for the epilogue, 128 bytes per row, the 16-byte piece k of row r
+//    at r 128 + 16 (k ^ r % 8).
 // ---------------------------------------------------------------------------
 constexpr int kTB = 128;               // query rows per CTA (the MMA M)
 constexpr int kSL = 32;                // source tokens per slice
