@@ -44,6 +44,35 @@ def test_reference_arm_line():
                         "d2h_bytes_per_step": 0}
 
 
+def test_traffic_records_keyed_to_kernel_code(tmp_path, monkeypatch):
+    """The ncu traffic record of a workload holds while the kernel code is the
+    code it was captured on: a comment or whitespace edit keeps the key, a code
+    edit (or a new source file) changes it, and the SSD and SSU keys are
+    independent of each other's sources."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    src = os.path.join(ROOT, "mamba2_ssm_decode_gb300", "csrc")
+    dst = tmp_path / "mamba2_ssm_decode_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for f in os.listdir(src):
+        if f.endswith((".cu", ".cuh")):
+            (dst / f).write_text(open(os.path.join(src, f), encoding="utf-8").read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    ssd, ssu = "ssd-prefill-2.7b", "mamba2-2.7b-decode"
+    base = {w: bench.kernel_source_hash(w) for w in (ssd, ssu)}
+    assert base[ssd] != base[ssu]
+    scan = dst / "ssd.cu"
+    text = scan.read_text()
+    scan.write_text("// a new comment line\n/* and a block\n comment */\n" + text.replace(";\n", ";  \n", 3))
+    assert {w: bench.kernel_source_hash(w) for w in (ssd, ssu)} == base
+    scan.write_text(text.replace("kSL = 32;", "kSL = 16;", 1))
+    assert bench.kernel_source_hash(ssd) != base[ssd] and bench.kernel_source_hash(ssu) == base[ssu]
+    scan.write_text(text)
+    (dst / "ssu_extra.cuh").write_text("int x;\n")
+    assert bench.kernel_source_hash(ssu) != base[ssu] and bench.kernel_source_hash(ssd) == base[ssd]
+
+
 def test_too_few_warmup_steps_rejected():
     r, d = run_bench("--steps", "3", "--warmup", "2", timeout=120)
     assert r.returncode != 0 and d is None
